@@ -1,0 +1,12 @@
+"""Synthetic workloads (shapes, shard splits, fusion groups, ranks) and
+their seeded source values. Shared by the tests, the benchmark and both
+sides of the parity check; holds none of the stage's arithmetic."""
+from .configs import (TILE, Output, Param, ValueRecipe, Workload, WORKLOADS, chunk_rows,
+                      edge_stress, kimi_k2_moe_layer, llama_dense, offload_layer, tiny_dense)
+from .values import make_shards, param_values, shards_to_host_u16, split_shards
+
+__all__ = [
+    "TILE", "Output", "Param", "ValueRecipe", "Workload", "WORKLOADS", "chunk_rows",
+    "edge_stress", "kimi_k2_moe_layer", "llama_dense", "offload_layer", "tiny_dense",
+    "make_shards", "param_values", "shards_to_host_u16", "split_shards",
+]

@@ -1,0 +1,254 @@
+"""Workload descriptors: parameter shapes, FSDP dim-0 shard splits, fusion
+groups, output formats and destination ranks.
+
+This module holds shapes and bookkeeping only; it does none of the stage's
+arithmetic. Both the CUDA library (through its binding) and the CPU oracle
+(through its own wrapper) receive the same descriptor and compute the
+layout and the outputs independently.
+
+The five named workloads mirror the shapes the stage is quoted on:
+a tiny two-layer dense transformer, a four-layer Llama-style stack, one
+Kimi-K2-shaped MoE layer (384 routed experts plus one shared expert,
+hidden 7168 -- the hidden size also appears on the page "Enabling
+trillion-parameter models on AWS EFA", section on dispatch/combine
+kernels), an edge/value-stress set, and an eight-layer CPU-offloaded stack.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+from typing import Optional, Sequence
+
+TILE = 128
+
+
+def chunk_rows(rows: int, shards: int) -> tuple:
+    """Dim-0 split with torch.chunk semantics: ceil(rows/shards) rows per
+    shard, the remainder in the last non-empty one; trailing shards that
+    get nothing are kept with 0 rows so every parameter has `shards`
+    entries (the FSDP placement of the page "Weight transfer for RL
+    post-training in under 2 seconds", section "DeviceMesh and mesh
+    groups", with empty shards allowed)."""
+    per = -(-rows // shards)
+    out, left = [], rows
+    for _ in range(shards):
+        n = min(per, left)
+        out.append(n)
+        left -= n
+    return tuple(out)
+
+
+@dataclass(frozen=True)
+class Param:
+    name: str
+    rows: int
+    cols: int
+    shard_rows: tuple
+
+    @property
+    def numel(self) -> int:
+        return self.rows * self.cols
+
+
+@dataclass(frozen=True)
+class Output:
+    name: str
+    parts: tuple            # param indices, fusion order
+    fp8: bool               # True: e4m3 + 128x128 fp32 scales; False: BF16 bytes
+    dst_ranks: tuple
+    data_off: Optional[tuple] = None    # None or per-destination offset / None=auto
+    scale_off: Optional[tuple] = None
+
+
+@dataclass(frozen=True)
+class ValueRecipe:
+    """How source values are drawn (see workloads.values)."""
+    dist: str = "normal"        # "normal" or "student_t3"
+    sigma: float = 0.02
+    seed: int = 0
+    zero_tile_eighths: int = 0      # blocks whose seeded hash % 8 lands here are all zero
+    outlier_tile_eighths: int = 0   # blocks that get one +-outlier
+    outlier: float = 3.0e4
+
+
+@dataclass
+class Workload:
+    name: str
+    params: list
+    outputs: list
+    num_ranks: int
+    values: ValueRecipe = field(default_factory=ValueRecipe)
+
+    # --- derived sizes (bookkeeping only) ---------------------------------
+    def output_shape(self, o: int) -> tuple:
+        out = self.outputs[o]
+        cols = {self.params[p].cols for p in out.parts}
+        if len(cols) != 1:
+            raise ValueError(f"fusion parts of {out.name} differ in cols")
+        return sum(self.params[p].rows for p in out.parts), cols.pop()
+
+    @property
+    def num_params_total(self) -> int:
+        return sum(p.numel for p in self.params)
+
+    @property
+    def bytes_read(self) -> int:
+        """BF16 source bytes read by one pass."""
+        return 2 * sum(self.params[p].numel for o in self.outputs for p in o.parts)
+
+    @property
+    def bytes_written(self) -> int:
+        """Destination bytes written by one pass (data + scales, all dsts)."""
+        total = 0
+        for o, out in enumerate(self.outputs):
+            m, n = self.output_shape(o)
+            per = m * n if out.fp8 else 2 * m * n
+            if out.fp8:
+                per += 4 * (-(-m // TILE)) * (-(-n // TILE))
+            total += per * len(out.dst_ranks)
+        return total
+
+    @property
+    def num_tiles(self) -> int:
+        t = 0
+        for o in range(len(self.outputs)):
+            m, n = self.output_shape(o)
+            t += (-(-m // TILE)) * (-(-n // TILE))
+        return t
+
+    def subset(self, outputs: Sequence[int], name: Optional[str] = None) -> "Workload":
+        """A workload made of some outputs (and only the params they use),
+        keeping each output's destination ranks."""
+        keep_params = []
+        for o in outputs:
+            for p in self.outputs[o].parts:
+                if p not in keep_params:
+                    keep_params.append(p)
+        remap = {p: i for i, p in enumerate(keep_params)}
+        outs = []
+        for o in outputs:
+            out = self.outputs[o]
+            outs.append(Output(out.name, tuple(remap[p] for p in out.parts), out.fp8,
+                               out.dst_ranks, out.data_off, out.scale_off))
+        return Workload(name or f"{self.name}[subset]", [self.params[p] for p in keep_params],
+                        outs, self.num_ranks, self.values)
+
+
+class _Builder:
+    def __init__(self, name, num_ranks, shards, values):
+        self.w = Workload(name, [], [], num_ranks, values)
+        self.shards = shards
+
+    def param(self, name, rows, cols, shard_rows=None):
+        sr = shard_rows if shard_rows is not None else chunk_rows(rows, self.shards)
+        self.w.params.append(Param(name, rows, cols, tuple(sr)))
+        return len(self.w.params) - 1
+
+    def output(self, name, parts, fp8, dst_ranks, data_off=None, scale_off=None):
+        self.w.outputs.append(Output(name, tuple(parts), fp8, tuple(dst_ranks),
+                                     data_off, scale_off))
+
+    def round_robin_rank(self):
+        """Outputs go round-robin over the ranks in plan order."""
+        return len(self.w.outputs) % self.w.num_ranks
+
+
+def dense_transformer(name, layers, hidden, q_heads, kv_heads, head_dim, ffn, vocab,
+                      shards, ranks, values, lm_head_fp8=True) -> Workload:
+    """Embedding (BF16), per layer [qkv, o, gate_up, down (FP8), two norms
+    (BF16, [hidden, 1])], final norm (BF16), untied lm_head (FP8 unless
+    lm_head_fp8 is False)."""
+    b = _Builder(name, ranks, shards, values)
+
+    def out(name, parts, fp8):
+        b.output(name, parts, fp8, (b.round_robin_rank(),))
+
+    out("embed", [b.param("embed", vocab, hidden)], False)
+    for l in range(layers):
+        q = b.param(f"l{l}.q", q_heads * head_dim, hidden)
+        k = b.param(f"l{l}.k", kv_heads * head_dim, hidden)
+        v = b.param(f"l{l}.v", kv_heads * head_dim, hidden)
+        out(f"l{l}.qkv", [q, k, v], True)
+        out(f"l{l}.o", [b.param(f"l{l}.o", hidden, q_heads * head_dim)], True)
+        g = b.param(f"l{l}.gate", ffn, hidden)
+        u = b.param(f"l{l}.up", ffn, hidden)
+        out(f"l{l}.gate_up", [g, u], True)
+        out(f"l{l}.down", [b.param(f"l{l}.down", hidden, ffn)], True)
+        out(f"l{l}.attn_norm", [b.param(f"l{l}.attn_norm", hidden, 1)], False)
+        out(f"l{l}.mlp_norm", [b.param(f"l{l}.mlp_norm", hidden, 1)], False)
+    out("final_norm", [b.param("final_norm", hidden, 1)], False)
+    out("lm_head", [b.param("lm_head", vocab, hidden)], lm_head_fp8)
+    return b.w
+
+
+def tiny_dense() -> Workload:
+    """Two layers, hidden 256, 4 q heads / 2 kv heads of 64, FFN 512,
+    vocab 1024, 4 shards, 2 destination ranks, N(0, 0.02), seed 1001."""
+    return dense_transformer("tiny_dense_2l_h256", 2, 256, 4, 2, 64, 512, 1024,
+                             shards=4, ranks=2, values=ValueRecipe("normal", 0.02, 1001))
+
+
+def llama_dense(lm_head_fp8=True) -> Workload:
+    """Four layers, hidden 4096, 32 q heads / 8 kv heads of 128, FFN 14336,
+    vocab 128256, 8 shards, 4 destination ranks, N(0, 0.02), seed 1002."""
+    return dense_transformer("llama_dense_4l_h4096", 4, 4096, 32, 8, 128, 14336, 128256,
+                             shards=8, ranks=4, values=ValueRecipe("normal", 0.02, 1002),
+                             lm_head_fp8=lm_head_fp8)
+
+
+def _moe_experts(b: _Builder, prefix: str, experts: int, hidden: int, inter: int,
+                 rank_of=None):
+    for e in range(experts):
+        rank = (e % b.w.num_ranks) if rank_of is None else rank_of(e)
+        w1 = b.param(f"{prefix}e{e}.w1", inter, hidden)
+        w3 = b.param(f"{prefix}e{e}.w3", inter, hidden)
+        b.output(f"{prefix}e{e}.gate_up", [w1, w3], True, (rank,))
+        w2 = b.param(f"{prefix}e{e}.w2", hidden, inter)
+        b.output(f"{prefix}e{e}.down", [w2], True, (rank,))
+
+
+def kimi_k2_moe_layer(experts: int = 385, seed: int = 1003) -> Workload:
+    """One Kimi-K2-shaped MoE layer: 384 routed experts plus the shared one
+    (index 384), each w1/w3 2048x7168 fused into gate_up 4096x7168 and w2
+    7168x2048, 8 dim-0 shards per weight, expert e on rank e % 8, all FP8,
+    N(0, 0.006). `experts` < 385 gives the first `experts` of them."""
+    b = _Builder(f"kimi_k2_moe_layer_e{experts}", 8, 8, ValueRecipe("normal", 0.006, seed))
+    _moe_experts(b, "", experts, 7168, 2048)
+    return b.w
+
+
+def edge_stress() -> Workload:
+    """7168x2050 (ragged last column block, 4100-byte rows) and 1000x7168
+    (ragged last row block) FP8, a 163840x7168 BF16 embedding, 3 uneven
+    shards each, 5 ranks of which 3 and 4 receive nothing. Values
+    Student-t(3) x 0.02; one block in eight all-zero, one in eight with a
+    single +-3e4 outlier. Seed 1004."""
+    vals = ValueRecipe("student_t3", 0.02, 1004, zero_tile_eighths=1,
+                       outlier_tile_eighths=1, outlier=3.0e4)
+    b = _Builder("edge_stress", 5, 3, vals)
+    b.output("A", [b.param("A", 7168, 2050)], True, (0,))
+    b.output("B", [b.param("B", 1000, 7168)], True, (1,))
+    b.output("C_embed", [b.param("C_embed", 163840, 7168)], False, (2,))
+    return b.w
+
+
+def offload_layer(experts: int = 385, seed: int = 1005) -> Workload:
+    """One layer of the streamed-offload stack: the MoE layer above plus
+    attention projections q, k, v, o of 7168x7168 (q/k/v fused into qkv
+    21504x7168), all FP8, 8 shards, 8 ranks."""
+    b = _Builder(f"offload_layer_e{experts}", 8, 8, ValueRecipe("normal", 0.006, seed))
+    q = b.param("q", 7168, 7168)
+    k = b.param("k", 7168, 7168)
+    v = b.param("v", 7168, 7168)
+    b.output("qkv", [q, k, v], True, (b.round_robin_rank(),))
+    b.output("o", [b.param("o", 7168, 7168)], True, (b.round_robin_rank(),))
+    _moe_experts(b, "", experts, 7168, 2048)
+    return b.w
+
+
+WORKLOADS = {
+    "tiny_dense": tiny_dense,
+    "llama_dense": llama_dense,
+    "kimi_k2_moe_layer": kimi_k2_moe_layer,
+    "edge_stress": edge_stress,
+    "offload_layer": offload_layer,
+}
