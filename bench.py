@@ -1,0 +1,371 @@
+"""Benchmark of wt_prepare on the Kimi-K2-shaped MoE layer (384 routed
+experts + 1 shared, w1/w3 2048x7168 fused to gate_up 4096x7168, w2
+7168x2048, 8 FSDP shards each, FP8 e4m3 128x128 blocks, 8 destination
+ranks; 16.96 G params, 33.9 GB BF16 read, 16.96 GB written per step).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+                  [--workload kimi_k2_moe_layer|offload_8layer] [--no-e2e]
+                  [--no-cpu-baseline] [--experts E]
+
+Prints one JSON line. `value` is GB/s of BF16 input for the whole job
+(all ranks), timed with CUDA events on the launching stream around K
+back-to-back steps whose inputs (33.9 GB) are far larger than L2. `e2e`
+is the same metric through wt_prepare_offload from pinned host memory,
+with the host-to-device copies and a device-to-host read of every
+destination pool inside the timed region. `--impl reference` times the CPU
+oracle on the host cores on a bounded sample of the same workload.
+Under torchrun each rank prepares its own layer (weak scaling, no
+collective on the data path).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "wt_prepare GB/s (BF16 in) and params/s at 1 B300; % of HBM roofline"
+GiB = 1 << 30
+SPEC_HBM_GBS = 8000.0
+
+# dram__bytes_read.sum + dram__bytes_write.sum of one prep_kernel launch,
+# from the ncu capture summarised in profiles/, scaled to the full layer;
+# valid only for the kernel source it was taken on.
+TRAFFIC = {"kernel_sha256": None, "bytes_per_launch": None}
+
+
+def kernel_sha() -> str:
+    with open(os.path.join(ROOT, "bf16_fp8_parameter_wt_b300", "csrc", "prep_kernel.cu"), "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()
+
+
+def measured_peaks() -> dict:
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f)
+    except OSError:
+        return {}
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, bus_id: str | None):
+        self.proc = None
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+               "-lms", "200"]
+        if bus_id:
+            cmd.insert(1, f"--id={bus_id}")
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self) -> dict | None:
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_setup():
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(world, v: float, dev) -> float:
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def cpu_baseline(w_full, experts_sample: int, steps: int = 1) -> dict:
+    """Time the CPU oracle, as it stands, on the first `experts_sample`
+    experts of the layer (same shapes, same value recipe)."""
+    import oracle
+    from workloads import make_shards, shards_to_host_u16
+    oracle.build()
+    sub = w_full.subset(range(2 * experts_sample), name=f"{w_full.name}[:{experts_sample} experts]")
+    host = shards_to_host_u16(make_shards(sub, device="cpu"))
+    m = oracle.Model(sub)
+    cores = max(1, len(os.sched_getaffinity(0)))
+    times = []
+    for _ in range(steps):
+        t0 = time.perf_counter()
+        m.prepare(host, nthreads=cores)
+        times.append(time.perf_counter() - t0)
+    t = statistics.median(times)
+    return {"value": round(sub.bytes_read / t / 1e9, 4), "unit": "GB/s", "cores": cores,
+            "kind": "oracle", "params_per_s": round(sub.num_params_total / t, 1),
+            "sample": f"{experts_sample} of {len(w_full.outputs) // 2} experts "
+                      f"({sub.num_params_total} params, {sub.bytes_read} B BF16 in), "
+                      f"median of {steps} run(s), {t:.2f} s each"}
+
+
+def run_reference(args, world, rank):
+    """The reference arm: the CPU oracle timed on the host cores."""
+    if rank != 0:
+        return
+    from workloads import kimi_k2_moe_layer
+    w = kimi_k2_moe_layer(args.experts)
+    import oracle
+    from workloads import make_shards, shards_to_host_u16
+    oracle.build()
+    sample_experts = args.reference_experts
+    sub = w.subset(range(2 * sample_experts))
+    host = shards_to_host_u16(make_shards(sub, device="cpu"))
+    m = oracle.Model(sub)
+    cores = max(1, len(os.sched_getaffinity(0)))
+    for _ in range(args.warmup):
+        m.prepare(host, nthreads=cores)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        m.prepare(host, nthreads=cores)
+    dt = (time.perf_counter() - t0) / args.steps
+    value = sub.bytes_read / dt / 1e9
+    sample = (f"each step: {sample_experts} of {len(w.outputs) // 2} experts "
+              f"({sub.num_params_total} params)")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded N(0, 0.006) BF16)",
+        "params_per_s": round(sub.num_params_total / dt, 1),
+        "config": {"workload": w.name, "experts": args.experts, "sample": sample,
+                   "parallelism": "replicas" if world > 1 else "single"},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="wt", choices=["wt", "reference"])
+    ap.add_argument("--experts", type=int, default=385)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--cpu-experts", type=int, default=8)
+    ap.add_argument("--reference-experts", type=int, default=2)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    world, rank, local = dist_setup() if args.impl == "wt" else (
+        int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")), 0)
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+        return
+
+    import torch
+    import bf16_fp8_parameter_wt_b300 as wt
+    from bf16_fp8_parameter_wt_b300 import build as wt_build
+    from workloads import kimi_k2_moe_layer, make_shards
+
+    wt_build.build()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    w = kimi_k2_moe_layer(args.experts, seed=1003 + rank)
+    shards = make_shards(w, device=dev)
+    flat = [s for per in shards for s in per]
+    shard_ptrs = [s.data_ptr() for s in flat]
+    plan = wt.Plan(w, device=local)
+    st = plan.stats
+    pools = [torch.empty(max(1, plan.pool_bytes(r)), dtype=torch.uint8, device=dev)
+             for r in range(w.num_ranks)]
+    pool_ptrs = [p.data_ptr() for p in pools]
+    stream = torch.cuda.Stream(dev)
+    sp = stream.cuda_stream
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            plan.prepare(shard_ptrs, pool_ptrs, sp)
+    stream.synchronize()
+
+    props = torch.cuda.get_device_properties(dev)
+    bus = None
+    try:
+        bus = f"{props.pci_domain_id:08X}:{props.pci_bus_id:02X}:{props.pci_device_id:02X}.0"
+    except AttributeError:
+        pass
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    clocks = ClockSampler(bus)
+    time.sleep(0.3)
+    t_wall = time.perf_counter()
+    for i in range(args.steps):
+        starts[i].record(stream)
+        plan.prepare(shard_ptrs, pool_ptrs, sp)
+        ends[i].record(stream)
+    stream.synchronize()
+    t_wall = time.perf_counter() - t_wall
+    barrier(world)
+    clk = clocks.stop()
+    per_launch_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    total_ms = starts[0].elapsed_time(ends[-1])
+    total_ms = max_over_ranks(world, total_ms, dev)
+    ms_per_step = total_ms / args.steps
+    value = world * st["bytes_read"] / (ms_per_step * 1e-3) / 1e9
+    params_per_s = world * st["num_params_total"] / (ms_per_step * 1e-3)
+    avg_launch_s = statistics.mean(per_launch_ms) * 1e-3
+    alg_bytes = st["bytes_read"] + st["bytes_written"]
+    peaks = measured_peaks()
+    peak = peaks.get("hbm_gbs")
+    achieved = alg_bytes / avg_launch_s / 1e9
+    traffic = TRAFFIC["bytes_per_launch"] if TRAFFIC["kernel_sha256"] == kernel_sha() else None
+    roofline = {"bound": "hbm", "achieved": round(achieved, 1),
+                "peak": peak if peak else 6400.0, "unit": "GB/s",
+                "frac": round(achieved / (peak if peak else 6400.0), 4),
+                "peak_source": "measured (MEASURED_PEAKS.json hbm_gbs)" if peak else "fallback",
+                "frac_of_8TBs_spec": round(achieved / SPEC_HBM_GBS, 4),
+                "traffic": traffic, "algorithmic_bytes_per_launch": alg_bytes,
+                "kernel": "prep_kernel", "launch_ms_median": round(statistics.median(per_launch_ms), 4),
+                "launch_ms_min": round(min(per_launch_ms), 4)}
+
+    e2e = None
+    if not args.no_e2e:
+        del pools
+        torch.cuda.empty_cache()
+        e2e = measure_e2e(w, shards, args, dev, world)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        del shards, flat
+        torch.cuda.empty_cache()
+        cpu = cpu_baseline(w, args.cpu_experts)
+
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded N(0, 0.006) BF16, generated on device)",
+        "params_per_s": round(params_per_s, 1),
+        "hbm_frac_of_8TBs_spec": round(value * (alg_bytes / st["bytes_read"]) / SPEC_HBM_GBS, 4),
+        "config": {"workload": w.name, "experts": args.experts, "params_per_rank": st["num_params_total"],
+                   "bytes_read_per_rank": st["bytes_read"], "bytes_written_per_rank": st["bytes_written"],
+                   "io": "BF16 in; e4m3 codes + fp32 128x128 scales out",
+                   "l2": "inputs (33.9 GB) larger than L2, no flush",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single"},
+        "roofline": roofline, "e2e": e2e, "cpu_baseline": cpu, "clocks": clk,
+        "gpu_launches": args.steps, "wall_s_timed": round(t_wall, 4),
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    plan.close()
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def measure_e2e(w, shards, args, dev, world):
+    """wt_prepare_offload from a pinned host image (2 GiB chunks) plus a
+    device-to-host read of every destination pool into pinned memory."""
+    import torch
+    import bf16_fp8_parameter_wt_b300 as wt
+    plan = wt.Plan(w, device=dev.index, offload_chunk_bytes=2 * GiB)
+    st = plan.stats
+    host = torch.empty(st["host_bytes"], dtype=torch.uint8, pin_memory=True)
+    for p, per in enumerate(shards):
+        for k, s in enumerate(per):
+            off = plan.shard_host_offset(p, k)
+            n = s.numel() * 2
+            host[off:off + n].copy_(s.view(torch.uint8).flatten())
+    pools = [torch.empty(max(1, plan.pool_bytes(r)), dtype=torch.uint8, device=dev)
+             for r in range(w.num_ranks)]
+    host_pools = [torch.empty(p.numel(), dtype=torch.uint8, pin_memory=True) for p in pools]
+    pool_ptrs = [p.data_ptr() for p in pools]
+    copy_s, comp_s = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+
+    def step():
+        plan.prepare_offload(host.data_ptr(), pool_ptrs, copy_s.cuda_stream, comp_s.cuda_stream)
+        with torch.cuda.stream(comp_s):
+            for hp, p in zip(host_pools, pools):
+                hp.copy_(p, non_blocking=True)
+        comp_s.synchronize()
+
+    step()
+    barrier(world)
+    t0 = time.perf_counter()
+    for _ in range(args.e2e_steps):
+        step()
+    dt = (time.perf_counter() - t0) / args.e2e_steps
+    dt = max_over_ranks(world, dt, dev)
+    # one plain pinned 2 GiB host-to-device copy: the bound of this path
+    buf = torch.empty(2 * GiB, dtype=torch.uint8, device=dev)
+    best = 0.0
+    for _ in range(3):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(copy_s)
+        with torch.cuda.stream(copy_s):
+            buf.copy_(host[:2 * GiB], non_blocking=True)
+        e1.record(copy_s)
+        copy_s.synchronize()
+        best = max(best, 2 * GiB / (e0.elapsed_time(e1) * 1e-3) / 1e9)
+    plan.close()
+    d2h = sum(p.numel() for p in pools)
+    return {"value": round(world * st["bytes_read"] / dt / 1e9, 3), "unit": "GB/s",
+            "h2d_bytes_per_step": st["host_bytes"], "d2h_bytes_per_step": d2h,
+            "ms_per_step": round(dt * 1e3, 2), "chunks": st["num_chunks"],
+            "h2d_peak_gbs": round(best, 2), "api": "wt_prepare_offload + pool D2H"}
+
+
+if __name__ == "__main__":
+    main()

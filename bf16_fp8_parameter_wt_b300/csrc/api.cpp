@@ -1,0 +1,403 @@
+// C ABI of the preparation library (declared in include/wt.h): plan
+// creation and upload, the per-step wt_prepare, the CPU-offload pipeline
+// (host-to-device copies on one stream overlapping preparation on another,
+// "Weight transfer for RL post-training in under 2 seconds", sections
+// "Task pipeline" and "GPU memory usage control"), checks and teardown.
+#include <algorithm>
+#include <cstring>
+#include <new>
+#include <string>
+
+#include "plan.h"
+
+namespace wt {
+
+namespace {
+thread_local std::string g_last_error;
+
+struct DeviceGuard {
+  int prev = -1;
+  bool ok = true;
+  explicit DeviceGuard(int dev) {
+    if (cudaGetDevice(&prev) != cudaSuccess) prev = -1;
+    if (prev != dev) ok = cudaSetDevice(dev) == cudaSuccess;
+  }
+  ~DeviceGuard() {
+    int cur = -1;
+    if (prev >= 0 && cudaGetDevice(&cur) == cudaSuccess && cur != prev) cudaSetDevice(prev);
+  }
+};
+
+wt_status fail(wt_status s, const std::string& msg) {
+  set_error(msg);
+  return s;
+}
+
+wt_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(WT_ERR_CUDA, std::string(what) + ": " + cudaGetErrorString(e));
+}
+
+size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
+
+void free_device(Plan& p) {
+  if (p.device < 0) return;
+  DeviceGuard g(p.device);
+  if (p.d_tables) cudaFree(p.d_tables);
+  if (p.h_pinned_ptrs) cudaFreeHost(p.h_pinned_ptrs);
+  for (int b = 0; b < 2; ++b) {
+    if (p.staging[b]) cudaFree(p.staging[b]);
+    if (p.h2d_done[b]) cudaEventDestroy(p.h2d_done[b]);
+    if (p.prep_done[b]) cudaEventDestroy(p.prep_done[b]);
+  }
+  if (p.ptr_upload_done) cudaEventDestroy(p.ptr_upload_done);
+  if (p.last_done) cudaEventDestroy(p.last_done);
+  p.d_tables = nullptr;
+  p.h_pinned_ptrs = nullptr;
+}
+
+// Upload the static tables and allocate what the per-step calls need, so
+// that wt_prepare and wt_prepare_offload never allocate.
+wt_status upload(Plan& p, int device) {
+  int count = 0;
+  cudaError_t e = cudaGetDeviceCount(&count);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDeviceCount");
+  if (device >= count) return fail(WT_ERR_INVALID_ARGUMENT, "device index out of range");
+  DeviceGuard g(device);
+  if (!g.ok) return fail(WT_ERR_CUDA, "cudaSetDevice failed");
+  p.device = device;
+  e = cudaDeviceGetAttribute(&p.sm_count, cudaDevAttrMultiProcessorCount, device);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+  p.grid_per_sm = prep_blocks_per_sm();
+
+  const size_t n_slots = (size_t)p.num_slots, n_ranks = (size_t)p.num_ranks;
+  const bool offload = p.chunk_bytes > 0;
+  size_t off = 0;
+  auto take = [&](size_t bytes) { size_t o = off; off = align256(off + bytes); return o; };
+  const size_t o_outs = take(p.h_outs.size() * sizeof(DevOutput));
+  const size_t o_runs = take(p.h_runs.size() * sizeof(DevRun));
+  const size_t o_trow = take(p.h_trow.size() * sizeof(int32_t));
+  const size_t o_dsts = take(p.h_dsts.size() * sizeof(DevDst));
+  const size_t o_unit = take(p.h_unit_out.size() * sizeof(uint32_t));
+  const size_t o_ptrs = take((n_slots + n_ranks) * sizeof(void*));   // shards, then pools
+  const size_t o_pbytes = take(n_ranks * sizeof(uint64_t));
+  const size_t o_err = take(sizeof(int32_t));
+  const size_t o_offl = take(offload ? n_slots * sizeof(void*) : 0);
+  e = cudaMalloc(&p.d_tables, std::max<size_t>(off, 256));
+  if (e != cudaSuccess) return fail(WT_ERR_OUT_OF_MEMORY, "cudaMalloc of plan tables failed");
+  char* base = static_cast<char*>(p.d_tables);
+  auto put = [&](size_t o, const void* src, size_t bytes) {
+    return bytes ? cudaMemcpy(base + o, src, bytes, cudaMemcpyHostToDevice) : cudaSuccess;
+  };
+  if ((e = put(o_outs, p.h_outs.data(), p.h_outs.size() * sizeof(DevOutput))) != cudaSuccess ||
+      (e = put(o_runs, p.h_runs.data(), p.h_runs.size() * sizeof(DevRun))) != cudaSuccess ||
+      (e = put(o_trow, p.h_trow.data(), p.h_trow.size() * sizeof(int32_t))) != cudaSuccess ||
+      (e = put(o_dsts, p.h_dsts.data(), p.h_dsts.size() * sizeof(DevDst))) != cudaSuccess ||
+      (e = put(o_unit, p.h_unit_out.data(), p.h_unit_out.size() * sizeof(uint32_t))) != cudaSuccess ||
+      (e = put(o_pbytes, p.pool_bytes.data(), n_ranks * sizeof(uint64_t))) != cudaSuccess ||
+      (e = cudaMemset(base + o_err, 0, sizeof(int32_t))) != cudaSuccess)
+    return cuda_fail(e, "uploading plan tables");
+  p.args.outs = reinterpret_cast<const DevOutput*>(base + o_outs);
+  p.args.runs = reinterpret_cast<const DevRun*>(base + o_runs);
+  p.args.trow_first_run = reinterpret_cast<const int32_t*>(base + o_trow);
+  p.args.dsts = reinterpret_cast<const DevDst*>(base + o_dsts);
+  p.args.unit_out = reinterpret_cast<const uint32_t*>(base + o_unit);
+  p.d_shard_ptrs = reinterpret_cast<const uint16_t**>(base + o_ptrs);
+  p.d_pool_ptrs = reinterpret_cast<uint8_t**>(base + o_ptrs + n_slots * sizeof(void*));
+  p.d_pool_bytes = reinterpret_cast<uint64_t*>(base + o_pbytes);
+  p.d_error = reinterpret_cast<int32_t*>(base + o_err);
+  p.args.pool_ptrs = p.d_pool_ptrs;
+  p.args.pool_bytes = p.d_pool_bytes;
+  p.args.error_word = p.d_error;
+
+  e = cudaHostAlloc(&p.h_pinned_ptrs, std::max<size_t>((n_slots + n_ranks) * sizeof(void*), 8),
+                    cudaHostAllocDefault);
+  if (e != cudaSuccess) return fail(WT_ERR_OUT_OF_MEMORY, "pinned pointer staging allocation failed");
+  if ((e = cudaEventCreateWithFlags(&p.ptr_upload_done, cudaEventDisableTiming)) != cudaSuccess ||
+      (e = cudaEventCreateWithFlags(&p.last_done, cudaEventDisableTiming)) != cudaSuccess)
+    return cuda_fail(e, "cudaEventCreate");
+  p.cached_shards.assign(n_slots, nullptr);
+  p.cached_pools.assign(n_ranks, nullptr);
+  p.ptrs_valid = false;
+
+  if (offload) {
+    // the watermark: two staging buffers of the largest chunk
+    for (int b = 0; b < 2; ++b) {
+      if (p.staging_bytes && cudaMalloc(&p.staging[b], p.staging_bytes) != cudaSuccess)
+        return fail(WT_ERR_OUT_OF_MEMORY, "offload staging allocation failed");
+      if ((e = cudaEventCreateWithFlags(&p.h2d_done[b], cudaEventDisableTiming)) != cudaSuccess ||
+          (e = cudaEventCreateWithFlags(&p.prep_done[b], cudaEventDisableTiming)) != cudaSuccess)
+        return cuda_fail(e, "cudaEventCreate");
+    }
+    // static shard table: chunk c's shards live in staging[c % 2]
+    std::vector<const void*> tbl(n_slots, nullptr);
+    for (size_t c = 0; c < p.chunks.size(); ++c) {
+      const Chunk& ch = p.chunks[c];
+      char* st = static_cast<char*>(p.staging[c % 2]);
+      for (int o = ch.out_begin; o < ch.out_end; ++o)
+        for (int32_t q : p.outputs[o].parts) {
+          const ParamInfo& pi = p.params[q];
+          for (size_t s = 0; s < pi.shard_rows.size(); ++s) {
+            const size_t slot = pi.slot_base + s;
+            tbl[slot] = st + (p.shard_host_off[slot] - ch.host_begin);
+          }
+        }
+    }
+    p.d_offload_shard_ptrs = reinterpret_cast<const uint16_t**>(base + o_offl);
+    if ((e = put(o_offl, tbl.data(), n_slots * sizeof(void*))) != cudaSuccess)
+      return cuda_fail(e, "uploading offload table");
+  }
+  return WT_OK;
+}
+
+// Check the caller's pool pointers and, when they or the shard pointers
+// changed since the last call, queue one copy of the pointer table on s.
+wt_status stage_pointers(Plan& p, const void* const* shards, void* const* pools, cudaStream_t s) {
+  const size_t n_slots = (size_t)p.num_slots, n_ranks = (size_t)p.num_ranks;
+  bool same = p.ptrs_valid;
+  if (same && pools) same = std::equal(p.cached_pools.begin(), p.cached_pools.end(), pools);
+  if (same && shards) same = std::equal(p.cached_shards.begin(), p.cached_shards.end(), shards);
+  if (same) return WT_OK;
+  for (size_t r = 0; r < n_ranks; ++r) {
+    if (p.pool_bytes[r] == 0) continue;
+    if (!pools[r]) return fail(WT_ERR_INVALID_ARGUMENT, "pool " + std::to_string(r) + " is NULL");
+    if (reinterpret_cast<uintptr_t>(pools[r]) % 16)
+      return fail(WT_ERR_ALIGNMENT, "pool " + std::to_string(r) + " is not 16-byte aligned");
+  }
+  if (shards) {
+    for (const ParamInfo& pi : p.params) {
+      const bool vec = p.outputs[pi.output].vec;
+      for (size_t k = 0; k < pi.shard_rows.size(); ++k) {
+        const void* ptr = shards[pi.slot_base + k];
+        if (pi.shard_rows[k] == 0) continue;
+        if (!ptr) return fail(WT_ERR_INVALID_ARGUMENT, pi.name + ": shard " + std::to_string(k) + " is NULL");
+        if (reinterpret_cast<uintptr_t>(ptr) % (vec ? 16 : 2))
+          return fail(WT_ERR_ALIGNMENT, pi.name + ": shard " + std::to_string(k) + " is misaligned");
+      }
+    }
+  }
+  // the pinned staging may still be read by the previous upload
+  cudaError_t e = cudaEventSynchronize(p.ptr_upload_done);
+  if (e != cudaSuccess) return cuda_fail(e, "waiting for the previous pointer upload");
+  const void** h = static_cast<const void**>(p.h_pinned_ptrs);
+  for (size_t i = 0; i < n_slots; ++i) h[i] = shards ? shards[i] : p.cached_shards[i];
+  for (size_t r = 0; r < n_ranks; ++r) h[n_slots + r] = pools[r];
+  if (n_slots + n_ranks) {
+    e = cudaMemcpyAsync(p.d_shard_ptrs, h, (n_slots + n_ranks) * sizeof(void*),
+                        cudaMemcpyHostToDevice, s);
+    if (e != cudaSuccess) return cuda_fail(e, "pointer table upload");
+  }
+  if ((e = cudaEventRecord(p.ptr_upload_done, s)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
+  if (shards) std::copy(shards, shards + n_slots, p.cached_shards.begin());
+  std::copy(pools, pools + n_ranks, p.cached_pools.begin());
+  // after an offload call the shard cache is not a valid image of the table
+  p.ptrs_valid = shards != nullptr;
+  return WT_OK;
+}
+
+int grid_for(const Plan& p, int64_t units) {
+  const int64_t full = (int64_t)p.sm_count * p.grid_per_sm;
+  return (int)std::max<int64_t>(1, std::min<int64_t>(units, full));
+}
+
+}  // namespace
+
+void set_error(const std::string& msg) { g_last_error = msg; }
+
+}  // namespace wt
+
+using namespace wt;
+
+extern "C" {
+
+wt_status wt_plan_create(const wt_plan_desc* desc, int device, wt_plan** out) {
+  if (!out) return fail(WT_ERR_INVALID_ARGUMENT, "out is NULL");
+  if (device < -1) return fail(WT_ERR_INVALID_ARGUMENT, "device must be >= -1");
+  wt_plan* h = new (std::nothrow) wt_plan;
+  if (!h) return fail(WT_ERR_OUT_OF_MEMORY, "host allocation failed");
+  wt_status st;
+  try {
+    st = compile_plan(desc, &h->p);
+  } catch (const std::bad_alloc&) {
+    st = fail(WT_ERR_OUT_OF_MEMORY, "host allocation failed");
+  }
+  if (st == WT_OK && device >= 0) {
+    st = upload(h->p, device);
+    if (st != WT_OK) free_device(h->p);
+  }
+  if (st != WT_OK) {
+    delete h;
+    return st;
+  }
+  *out = h;
+  return WT_OK;
+}
+
+wt_status wt_plan_pool_bytes(const wt_plan* h, int32_t rank, uint64_t* bytes) {
+  if (!h || !bytes) return fail(WT_ERR_INVALID_ARGUMENT, "NULL argument");
+  if (rank < 0 || rank >= h->p.num_ranks) return fail(WT_ERR_INVALID_ARGUMENT, "rank out of range");
+  *bytes = h->p.pool_bytes[rank];
+  return WT_OK;
+}
+
+wt_status wt_plan_output_layout(const wt_plan* h, int32_t out, int32_t dst, int32_t* rank,
+                                uint64_t* data_off, uint64_t* scale_off) {
+  if (!h || !rank || !data_off || !scale_off) return fail(WT_ERR_INVALID_ARGUMENT, "NULL argument");
+  if (out < 0 || out >= (int32_t)h->p.outputs.size()) return fail(WT_ERR_INVALID_ARGUMENT, "output out of range");
+  const OutputInfo& oi = h->p.outputs[out];
+  if (dst < 0 || dst >= (int32_t)oi.dsts.size()) return fail(WT_ERR_INVALID_ARGUMENT, "destination out of range");
+  *rank = oi.dsts[dst].rank;
+  *data_off = oi.dsts[dst].data_off;
+  *scale_off = oi.dsts[dst].scale_off;
+  return WT_OK;
+}
+
+wt_status wt_plan_shard_host_offset(const wt_plan* h, int32_t param, int32_t shard, uint64_t* off) {
+  if (!h || !off) return fail(WT_ERR_INVALID_ARGUMENT, "NULL argument");
+  if (param < 0 || param >= (int32_t)h->p.params.size()) return fail(WT_ERR_INVALID_ARGUMENT, "param out of range");
+  const ParamInfo& pi = h->p.params[param];
+  if (shard < 0 || shard >= (int32_t)pi.shard_rows.size()) return fail(WT_ERR_INVALID_ARGUMENT, "shard out of range");
+  *off = h->p.shard_host_off[pi.slot_base + shard];
+  return WT_OK;
+}
+
+wt_status wt_plan_get_stats(const wt_plan* h, wt_plan_stats* st) {
+  if (!h || !st) return fail(WT_ERR_INVALID_ARGUMENT, "NULL argument");
+  st->num_units = h->p.num_units;
+  st->num_params_total = h->p.num_params_total;
+  st->bytes_read = h->p.bytes_read;
+  st->bytes_written = h->p.bytes_written;
+  st->host_bytes = h->p.host_bytes;
+  st->num_chunks = (int32_t)h->p.chunks.size();
+  st->num_slots = h->p.num_slots;
+  return WT_OK;
+}
+
+wt_status wt_prepare(wt_plan* h, const void* const* shard_ptrs, void* const* pools, void* stream) {
+  if (!h) return fail(WT_ERR_INVALID_ARGUMENT, "plan is NULL");
+  Plan& p = h->p;
+  if (p.device < 0) return fail(WT_ERR_INVALID_ARGUMENT, "host-only plan cannot run");
+  if ((p.num_slots > 0 && !shard_ptrs) || (p.num_ranks > 0 && !pools))
+    return fail(WT_ERR_INVALID_ARGUMENT, "shard_ptrs or pools is NULL");
+  DeviceGuard g(p.device);
+  if (!g.ok) return fail(WT_ERR_CUDA, "cudaSetDevice failed");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  wt_status st = stage_pointers(p, shard_ptrs, pools, s);
+  if (st != WT_OK) return st;
+  PrepArgs a = p.args;
+  a.shard_ptrs = p.d_shard_ptrs;
+  a.unit_begin = 0;
+  a.unit_end = p.num_units;
+  cudaError_t e = launch_prepare(a, grid_for(p, p.num_units), s, p.flags & WT_FLAG_DEBUG_CHECKS);
+  if (e != cudaSuccess) return cuda_fail(e, "preparation kernel launch");
+  if ((e = cudaEventRecord(p.last_done, s)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
+  p.ran = true;
+  return WT_OK;
+}
+
+wt_status wt_prepare_offload(wt_plan* h, const void* host_image, void* const* pools,
+                             void* copy_stream, void* compute_stream) {
+  if (!h) return fail(WT_ERR_INVALID_ARGUMENT, "plan is NULL");
+  Plan& p = h->p;
+  if (p.device < 0) return fail(WT_ERR_INVALID_ARGUMENT, "host-only plan cannot run");
+  if (p.chunk_bytes == 0) return fail(WT_ERR_INVALID_ARGUMENT, "plan was built without offload_chunk_bytes");
+  if ((p.host_bytes > 0 && !host_image) || (p.num_ranks > 0 && !pools))
+    return fail(WT_ERR_INVALID_ARGUMENT, "host_image or pools is NULL");
+  DeviceGuard g(p.device);
+  if (!g.ok) return fail(WT_ERR_CUDA, "cudaSetDevice failed");
+  cudaStream_t cs = static_cast<cudaStream_t>(copy_stream);
+  cudaStream_t ks = static_cast<cudaStream_t>(compute_stream);
+  wt_status st = stage_pointers(p, nullptr, pools, ks);
+  if (st != WT_OK) return st;
+  PrepArgs a = p.args;
+  a.shard_ptrs = p.d_offload_shard_ptrs;
+  const char* host = static_cast<const char*>(host_image);
+  auto drain = [&](wt_status s_, const std::string& msg) {
+    cudaStreamSynchronize(cs);
+    cudaStreamSynchronize(ks);
+    return fail(s_, msg);
+  };
+  cudaError_t e;
+  for (size_t i = 0; i < p.chunks.size(); ++i) {
+    const Chunk& c = p.chunks[i];
+    const int b = (int)(i & 1);
+    if ((int32_t)i == p.fail_chunk)
+      return drain(WT_ERR_CUDA, "injected failure before queueing chunk " + std::to_string(i));
+    // the staging buffer is free once the preparation that last read it ended
+    if (p.prep_recorded[b] && (e = cudaStreamWaitEvent(cs, p.prep_done[b], 0)) != cudaSuccess)
+      return drain(WT_ERR_CUDA, std::string("cudaStreamWaitEvent: ") + cudaGetErrorString(e));
+    if (c.host_bytes &&
+        (e = cudaMemcpyAsync(p.staging[b], host + c.host_begin, c.host_bytes,
+                             cudaMemcpyHostToDevice, cs)) != cudaSuccess)
+      return drain(WT_ERR_CUDA, std::string("host-to-device copy: ") + cudaGetErrorString(e));
+    if ((e = cudaEventRecord(p.h2d_done[b], cs)) != cudaSuccess ||
+        (e = cudaStreamWaitEvent(ks, p.h2d_done[b], 0)) != cudaSuccess)
+      return drain(WT_ERR_CUDA, std::string("event: ") + cudaGetErrorString(e));
+    a.unit_begin = c.unit_begin;
+    a.unit_end = c.unit_end;
+    if ((e = launch_prepare(a, grid_for(p, c.unit_end - c.unit_begin), ks,
+                            p.flags & WT_FLAG_DEBUG_CHECKS)) != cudaSuccess)
+      return drain(WT_ERR_CUDA, std::string("preparation kernel launch: ") + cudaGetErrorString(e));
+    if ((e = cudaEventRecord(p.prep_done[b], ks)) != cudaSuccess)
+      return drain(WT_ERR_CUDA, std::string("cudaEventRecord: ") + cudaGetErrorString(e));
+    p.prep_recorded[b] = true;
+  }
+  if ((e = cudaEventRecord(p.last_done, ks)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
+  p.ran = true;
+  return WT_OK;
+}
+
+wt_status wt_plan_check(wt_plan* h, void* stream) {
+  if (!h) return fail(WT_ERR_INVALID_ARGUMENT, "plan is NULL");
+  Plan& p = h->p;
+  if (p.device < 0) return fail(WT_ERR_INVALID_ARGUMENT, "host-only plan");
+  DeviceGuard g(p.device);
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  int32_t word = 0;
+  if ((e = cudaMemcpy(&word, p.d_error, sizeof word, cudaMemcpyDeviceToHost)) != cudaSuccess)
+    return cuda_fail(e, "reading the error word");
+  if (word) {
+    cudaMemset(p.d_error, 0, sizeof(int32_t));
+    return fail(WT_ERR_INTERNAL, "a store fell outside its destination range");
+  }
+  return WT_OK;
+}
+
+wt_status wt_debug_fail_offload_chunk(wt_plan* h, int32_t chunk) {
+  if (!h) return fail(WT_ERR_INVALID_ARGUMENT, "plan is NULL");
+  h->p.fail_chunk = chunk;
+  return WT_OK;
+}
+
+wt_status wt_plan_destroy(wt_plan* h) {
+  if (!h) return WT_OK;
+  wt_status st = WT_OK;
+  if (h->p.device >= 0 && h->p.ran) {
+    DeviceGuard g(h->p.device);
+    cudaError_t e = cudaEventSynchronize(h->p.last_done);
+    if (e != cudaSuccess) st = cuda_fail(e, "waiting for the plan's last step");
+  }
+  free_device(h->p);
+  delete h;
+  return st;
+}
+
+const char* wt_status_string(wt_status s) {
+  switch (s) {
+    case WT_OK: return "WT_OK";
+    case WT_ERR_INVALID_ARGUMENT: return "WT_ERR_INVALID_ARGUMENT";
+    case WT_ERR_SHAPE: return "WT_ERR_SHAPE";
+    case WT_ERR_LAYOUT_OVERLAP: return "WT_ERR_LAYOUT_OVERLAP";
+    case WT_ERR_POOL_TOO_SMALL: return "WT_ERR_POOL_TOO_SMALL";
+    case WT_ERR_ALIGNMENT: return "WT_ERR_ALIGNMENT";
+    case WT_ERR_OUT_OF_MEMORY: return "WT_ERR_OUT_OF_MEMORY";
+    case WT_ERR_CUDA: return "WT_ERR_CUDA";
+    case WT_ERR_TIMEOUT: return "WT_ERR_TIMEOUT";
+    case WT_ERR_INTERNAL: return "WT_ERR_INTERNAL";
+  }
+  return "WT_ERR_UNKNOWN";
+}
+
+const char* wt_last_error(void) { return g_last_error.c_str(); }
+
+}  // extern "C"

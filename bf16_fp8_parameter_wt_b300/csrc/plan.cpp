@@ -1,0 +1,292 @@
+// Plan compiler: validates the descriptor and turns it into the static
+// schedule that every wt_prepare replays ("Weight transfer for RL
+// post-training in under 2 seconds", sections "High-level workflow" --
+// metadata in, schedule computed by the controller -- and "Why it is fast
+// and simple / static schedule" -- computed once, replayed each step).
+#include <algorithm>
+#include <cstdio>
+#include <cstring>
+#include <limits>
+
+#include "plan.h"
+
+namespace wt {
+
+namespace {
+
+uint64_t align_up(uint64_t v, uint64_t a) { return (v + a - 1) / a * a; }
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+std::string pname(const wt_param_desc& d, int i) {
+  return d.name ? std::string(d.name) : "param " + std::to_string(i);
+}
+std::string oname(const wt_output_desc& d, int i) {
+  return d.name ? std::string(d.name) : "output " + std::to_string(i);
+}
+
+wt_status fail(wt_status s, const std::string& msg) {
+  set_error(msg);
+  return s;
+}
+
+struct Range {
+  uint64_t off, bytes;
+  int32_t out, dst;
+  bool scale;
+};
+
+}  // namespace
+
+wt_status compile_plan(const wt_plan_desc* d, Plan* p) {
+  const int64_t kMaxDim = int64_t(1) << 40;
+  if (!d) return fail(WT_ERR_INVALID_ARGUMENT, "descriptor is NULL");
+  if (d->num_params < 0 || d->num_outputs < 0 || d->num_ranks < 0)
+    return fail(WT_ERR_INVALID_ARGUMENT, "negative count in descriptor");
+  if ((d->num_params > 0 && !d->params) || (d->num_outputs > 0 && !d->outputs))
+    return fail(WT_ERR_INVALID_ARGUMENT, "params/outputs array is NULL");
+  if (d->flags & ~(WT_FLAG_FORCE_NARROW | WT_FLAG_DEBUG_CHECKS))
+    return fail(WT_ERR_INVALID_ARGUMENT, "unknown flag bits");
+  p->flags = d->flags;
+  p->num_ranks = d->num_ranks;
+
+  // ---- params: shapes and dim-0 shards ---------------------------------
+  p->params.resize(d->num_params);
+  int64_t slot = 0;
+  for (int i = 0; i < d->num_params; ++i) {
+    const wt_param_desc& pd = d->params[i];
+    ParamInfo& pi = p->params[i];
+    pi.name = pname(pd, i);
+    if (pd.rows < 0 || pd.cols < 1 || pd.rows > kMaxDim || pd.cols > kMaxDim)
+      return fail(WT_ERR_SHAPE, pi.name + ": rows must be >= 0 and cols >= 1");
+    if (pd.num_shards < 1 || !pd.shard_rows)
+      return fail(WT_ERR_INVALID_ARGUMENT, pi.name + ": needs at least one shard");
+    int64_t sum = 0;
+    for (int s = 0; s < pd.num_shards; ++s) {
+      if (pd.shard_rows[s] < 0) return fail(WT_ERR_SHAPE, pi.name + ": negative shard rows");
+      sum += pd.shard_rows[s];
+    }
+    if (sum != pd.rows)
+      return fail(WT_ERR_SHAPE, pi.name + ": shard rows sum to " + std::to_string(sum) +
+                                    ", expected " + std::to_string(pd.rows));
+    pi.rows = pd.rows;
+    pi.cols = pd.cols;
+    pi.shard_rows.assign(pd.shard_rows, pd.shard_rows + pd.num_shards);
+    pi.slot_base = (int32_t)slot;
+    slot += pd.num_shards;
+    if (slot > std::numeric_limits<int32_t>::max())
+      return fail(WT_ERR_INVALID_ARGUMENT, "too many shards");
+    p->num_params_total += pd.rows * pd.cols;
+  }
+  p->num_slots = (int32_t)slot;
+
+  // ---- outputs: fusion groups, formats, destinations --------------------
+  p->outputs.resize(d->num_outputs);
+  int64_t units = 0;
+  for (int o = 0; o < d->num_outputs; ++o) {
+    const wt_output_desc& od = d->outputs[o];
+    OutputInfo& oi = p->outputs[o];
+    oi.name = oname(od, o);
+    if (od.num_parts < 1 || !od.part_params)
+      return fail(WT_ERR_INVALID_ARGUMENT, oi.name + ": needs at least one part");
+    if (od.format != WT_OUT_BF16 && od.format != WT_OUT_FP8_E4M3_B128)
+      return fail(WT_ERR_INVALID_ARGUMENT, oi.name + ": unknown format");
+    if (od.num_dsts < 1 || !od.dst_ranks)
+      return fail(WT_ERR_INVALID_ARGUMENT, oi.name + ": needs at least one destination");
+    oi.format = od.format;
+    int64_t rows = 0, cols = -1;
+    for (int k = 0; k < od.num_parts; ++k) {
+      int32_t q = od.part_params[k];
+      if (q < 0 || q >= d->num_params)
+        return fail(WT_ERR_INVALID_ARGUMENT, oi.name + ": part index out of range");
+      ParamInfo& pi = p->params[q];
+      if (pi.output >= 0)
+        return fail(WT_ERR_INVALID_ARGUMENT,
+                    pi.name + ": used by more than one output (or twice in one)");
+      pi.output = o;
+      if (cols < 0) cols = pi.cols;
+      if (pi.cols != cols)
+        return fail(WT_ERR_SHAPE, oi.name + ": fusion parts differ in cols");
+      rows += pi.rows;
+      oi.parts.push_back(q);
+    }
+    if (rows < 1 || rows > kMaxDim)
+      return fail(WT_ERR_SHAPE, oi.name + ": fused tensor has no rows");
+    if (rows * cols > (int64_t(1) << 46))
+      return fail(WT_ERR_SHAPE, oi.name + ": tensor too large");
+    oi.rows = rows;
+    oi.cols = cols;
+    const bool fp8 = od.format == WT_OUT_FP8_E4M3_B128;
+    oi.data_bytes = uint64_t(rows * cols) * (fp8 ? 1u : 2u);
+    oi.scale_bytes = fp8 ? uint64_t(ceil_div(rows, kTile) * ceil_div(cols, kTile)) * 4u : 0u;
+    oi.unit_begin = units;
+    oi.num_units = ceil_div(rows, kTile) * ceil_div(cols, kTile);
+    units += oi.num_units;
+    oi.vec = (cols % 8 == 0) && !(d->flags & WT_FLAG_FORCE_NARROW);
+    oi.dsts.resize(od.num_dsts);
+    for (int k = 0; k < od.num_dsts; ++k) {
+      int32_t r = od.dst_ranks[k];
+      if (r < 0 || r >= d->num_ranks)
+        return fail(WT_ERR_INVALID_ARGUMENT, oi.name + ": destination rank out of range");
+      oi.dsts[k].rank = r;
+      uint64_t doff = od.dst_data_off ? od.dst_data_off[k] : WT_OFFSET_AUTO;
+      uint64_t soff = (fp8 && od.dst_scale_off) ? od.dst_scale_off[k] : WT_OFFSET_AUTO;
+      if (doff != WT_OFFSET_AUTO && doff % 16)
+        return fail(WT_ERR_ALIGNMENT, oi.name + ": explicit data offset not a multiple of 16");
+      if (soff != WT_OFFSET_AUTO && soff % 4)
+        return fail(WT_ERR_ALIGNMENT, oi.name + ": explicit scale offset not a multiple of 4");
+      if ((doff != WT_OFFSET_AUTO && doff > (uint64_t(1) << 56)) ||
+          (soff != WT_OFFSET_AUTO && soff > (uint64_t(1) << 56)))
+        return fail(WT_ERR_INVALID_ARGUMENT, oi.name + ": explicit offset out of range");
+      oi.dsts[k].data_off = doff;
+      oi.dsts[k].scale_off = soff;
+    }
+    p->bytes_written += (oi.data_bytes + oi.scale_bytes) * (uint64_t)od.num_dsts;
+    p->bytes_read += uint64_t(rows * cols) * 2u;
+  }
+  for (int i = 0; i < d->num_params; ++i)
+    if (p->params[i].output < 0)
+      return fail(WT_ERR_INVALID_ARGUMENT, p->params[i].name + ": not used by any output");
+  p->num_units = units;
+  if (units > std::numeric_limits<uint32_t>::max() / 2)
+    return fail(WT_ERR_SHAPE, "too many 128x128 units");
+
+  // ---- destination layout: explicit ranges, then auto-pack per rank ------
+  p->pool_bytes.assign(d->num_ranks, 0);
+  std::vector<uint64_t> cursor(d->num_ranks, 0);
+  for (auto& oi : p->outputs)
+    for (auto& ds : oi.dsts) {
+      if (ds.data_off != WT_OFFSET_AUTO)
+        cursor[ds.rank] = std::max(cursor[ds.rank], ds.data_off + oi.data_bytes);
+      if (oi.format == WT_OUT_FP8_E4M3_B128 && ds.scale_off != WT_OFFSET_AUTO)
+        cursor[ds.rank] = std::max(cursor[ds.rank], ds.scale_off + oi.scale_bytes);
+    }
+  for (auto& oi : p->outputs)
+    for (auto& ds : oi.dsts) {
+      uint64_t& c = cursor[ds.rank];
+      if (ds.data_off == WT_OFFSET_AUTO) {
+        ds.data_off = align_up(c, 256);
+        c = ds.data_off + oi.data_bytes;
+      }
+      if (oi.format == WT_OUT_FP8_E4M3_B128) {
+        if (ds.scale_off == WT_OFFSET_AUTO) {
+          ds.scale_off = align_up(c, 256);
+          c = ds.scale_off + oi.scale_bytes;
+        }
+      } else {
+        ds.scale_off = 0;
+      }
+    }
+  // prove the ranges of every rank disjoint, and size the pools
+  std::vector<std::vector<Range>> per_rank(d->num_ranks);
+  for (int o = 0; o < (int)p->outputs.size(); ++o) {
+    auto& oi = p->outputs[o];
+    for (int k = 0; k < (int)oi.dsts.size(); ++k) {
+      auto& ds = oi.dsts[k];
+      per_rank[ds.rank].push_back({ds.data_off, oi.data_bytes, o, k, false});
+      if (oi.format == WT_OUT_FP8_E4M3_B128)
+        per_rank[ds.rank].push_back({ds.scale_off, oi.scale_bytes, o, k, true});
+    }
+  }
+  for (int r = 0; r < d->num_ranks; ++r) {
+    auto& v = per_rank[r];
+    std::sort(v.begin(), v.end(), [](const Range& a, const Range& b) { return a.off < b.off; });
+    uint64_t end = 0;
+    for (size_t i = 0; i < v.size(); ++i) {
+      if (i > 0 && v[i].off < v[i - 1].off + v[i - 1].bytes)
+        return fail(WT_ERR_LAYOUT_OVERLAP,
+                    "rank " + std::to_string(r) + ": destination of " +
+                        p->outputs[v[i].out].name + " overlaps " +
+                        p->outputs[v[i - 1].out].name);
+      end = std::max(end, v[i].off + v[i].bytes);
+    }
+    p->pool_bytes[r] = end ? align_up(end, 256) : 0;
+    if (d->pool_capacity && p->pool_bytes[r] > d->pool_capacity[r])
+      return fail(WT_ERR_POOL_TOO_SMALL, "rank " + std::to_string(r) + ": needs " +
+                                             std::to_string(p->pool_bytes[r]) + " bytes");
+  }
+
+  // ---- device tables: outputs, row runs, tile rows, destinations, units ---
+  p->h_outs.clear();
+  p->h_runs.clear();
+  p->h_trow.clear();
+  p->h_dsts.clear();
+  p->h_unit_out.assign((size_t)units, 0);
+  for (int o = 0; o < (int)p->outputs.size(); ++o) {
+    auto& oi = p->outputs[o];
+    DevOutput dv{};
+    dv.rows = oi.rows;
+    dv.cols = oi.cols;
+    dv.unit_begin = oi.unit_begin;
+    dv.tiles_n = (int32_t)ceil_div(oi.cols, kTile);
+    dv.fp8 = oi.format == WT_OUT_FP8_E4M3_B128;
+    dv.vec = oi.vec;
+    dv.num_dsts = (int32_t)oi.dsts.size();
+    dv.dst_begin = (int32_t)p->h_dsts.size();
+    dv.trow_begin = (int32_t)p->h_trow.size();
+    for (auto& ds : oi.dsts) p->h_dsts.push_back({ds.rank, 0, ds.data_off, ds.scale_off});
+    // the runs of this output: shards of its parts in fusion order, empty
+    // shards skipped (reassembly = row r of the part comes from the shard
+    // whose row range holds r)
+    const size_t first_run = p->h_runs.size();
+    int64_t row = 0;
+    for (int32_t q : oi.parts) {
+      auto& pi = p->params[q];
+      for (size_t s = 0; s < pi.shard_rows.size(); ++s) {
+        if (pi.shard_rows[s] == 0) continue;
+        p->h_runs.push_back({row, pi.shard_rows[s], pi.slot_base + (int32_t)s, 0});
+        row += pi.shard_rows[s];
+      }
+    }
+    size_t k = first_run;
+    for (int64_t bi = 0; bi * kTile < oi.rows; ++bi) {
+      while (p->h_runs[k].row0 + p->h_runs[k].rows <= bi * kTile) ++k;
+      p->h_trow.push_back((int32_t)k);
+    }
+    for (int64_t u = 0; u < oi.num_units; ++u) p->h_unit_out[oi.unit_begin + u] = (uint32_t)o;
+    p->h_outs.push_back(dv);
+  }
+
+  // ---- packed host image for offload and its chunks ----------------------
+  p->shard_host_off.assign(p->num_slots, 0);
+  uint64_t hcur = 0;
+  std::vector<uint64_t> out_host_begin(p->outputs.size() + 1, 0);
+  for (int o = 0; o < (int)p->outputs.size(); ++o) {
+    auto& oi = p->outputs[o];
+    out_host_begin[o] = hcur;
+    for (int32_t q : oi.parts) {
+      auto& pi = p->params[q];
+      for (size_t s = 0; s < pi.shard_rows.size(); ++s) {
+        hcur = align_up(hcur, 256);
+        p->shard_host_off[pi.slot_base + s] = hcur;
+        hcur += uint64_t(pi.shard_rows[s] * pi.cols) * 2u;
+      }
+    }
+    hcur = align_up(hcur, 256);
+  }
+  out_host_begin[p->outputs.size()] = hcur;
+  p->host_bytes = hcur;
+  p->chunk_bytes = d->offload_chunk_bytes;
+  p->chunks.clear();
+  p->staging_bytes = 0;
+  if (p->chunk_bytes > 0) {
+    int o = 0;
+    const int n = (int)p->outputs.size();
+    while (o < n) {
+      Chunk c;
+      c.out_begin = o;
+      c.host_begin = out_host_begin[o];
+      int e = o + 1;
+      while (e < n && out_host_begin[e + 1] - c.host_begin <= p->chunk_bytes) ++e;
+      c.out_end = e;
+      c.host_bytes = out_host_begin[e] - c.host_begin;
+      c.unit_begin = p->outputs[o].unit_begin;
+      c.unit_end = p->outputs[e - 1].unit_begin + p->outputs[e - 1].num_units;
+      p->staging_bytes = std::max(p->staging_bytes, c.host_bytes);
+      p->chunks.push_back(c);
+      o = e;
+    }
+  }
+  return WT_OK;
+}
+
+}  // namespace wt

@@ -1,0 +1,223 @@
+/*
+ * wt.h -- C ABI of the B300 parameter-preparation library.
+ *
+ * The stage this library runs is "parameter preparation" from the page
+ * "Weight transfer for RL post-training in under 2 seconds" (Perplexity):
+ *   - section "Task pipeline": per parameter, rebuild the full weight from
+ *     its shards (full_tensor()), apply projection fusion, quantize if the
+ *     destination needs it;
+ *   - section "DeviceMesh and mesh groups": parameters are FSDP-sharded
+ *     along dim 0;
+ *   - section "High-level workflow" and "Why it is fast and simple /
+ *     static schedule": the controller computes a static transfer schedule
+ *     once at start-up and every step only replays it;
+ *   - section "RDMA WRITE: one-sided transfers": a write is addressed by a
+ *     destination memory region and an offset in it.
+ * The inference side stores FP8 (page intro). Here FP8 means e4m3 ("fn":
+ * bias 7, no infinities, largest finite 448) with one fp32 scale per
+ * 128x128 block: scale = amax/448 (1.0 for an all-zero block), each code =
+ * e4m3_rne_satfinite(x / scale) with an IEEE binary32 division.
+ *
+ * Destination "memory regions" are caller-owned device buffers ("pools"),
+ * one per destination rank, on the plan's device. The remote RDMA write of
+ * the pages is out of scope: the library's coalesced stores into the pools
+ * stand in for it.
+ *
+ * Conventions for every call:
+ *   - Every call returns wt_status. Out-parameters are written only on
+ *     WT_OK. wt_last_error() gives a human-readable detail for the calling
+ *     thread's last failure.
+ *   - Device pointers are plain addresses on the plan's device. Streams are
+ *     cudaStream_t values passed as void* (NULL = the legacy default
+ *     stream).
+ *   - Nothing here synchronises the device unless documented.
+ */
+#ifndef WT_H
+#define WT_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  WT_OK = 0,
+  WT_ERR_INVALID_ARGUMENT = 1, /* null/out-of-range argument, bad index      */
+  WT_ERR_SHAPE = 2,            /* shard rows do not sum, fused cols differ   */
+  WT_ERR_LAYOUT_OVERLAP = 3,   /* destination ranges intersect               */
+  WT_ERR_POOL_TOO_SMALL = 4,   /* layout exceeds a given pool capacity       */
+  WT_ERR_ALIGNMENT = 5,        /* pointer/offset not aligned as required     */
+  WT_ERR_OUT_OF_MEMORY = 6,    /* device or pinned allocation failed         */
+  WT_ERR_CUDA = 7,             /* a CUDA runtime call failed                 */
+  WT_ERR_TIMEOUT = 8,          /* a bounded wait gave up                     */
+  WT_ERR_INTERNAL = 9          /* a debug check in a kernel fired            */
+} wt_status;
+
+typedef enum {
+  WT_OUT_BF16 = 0,          /* pass-through: the fused BF16 bytes           */
+  WT_OUT_FP8_E4M3_B128 = 1  /* e4m3 codes + fp32 scale per 128x128 block    */
+} wt_out_format;
+
+/* An offset that the plan chooses (auto-pack). */
+#define WT_OFFSET_AUTO UINT64_MAX
+
+/* Plan flags. */
+#define WT_FLAG_FORCE_NARROW 0x1u /* use the element-wise path everywhere (testing) */
+#define WT_FLAG_DEBUG_CHECKS 0x2u /* bounds-check every store; see wt_plan_check   */
+
+/* One source parameter: a rows x cols BF16 row-major tensor split along
+ * dim 0 into num_shards contiguous shards of shard_rows[i] rows each
+ * (FSDP placement; a shard may hold 0 rows). A 1-D tensor is cols = 1. */
+typedef struct {
+  const char* name;         /* optional, for messages; may be NULL */
+  int64_t rows, cols;
+  int32_t num_shards;
+  const int64_t* shard_rows;
+} wt_param_desc;
+
+/* One output tensor: the row concatenation of part_params in that order
+ * (projection fusion: q,k,v -> qkv; gate,up -> gate_up), written in
+ * `format` to each of num_dsts destinations (rank, data offset, scale
+ * offset). dst_data_off / dst_scale_off may be NULL (all automatic) or hold
+ * WT_OFFSET_AUTO entries. Explicit data offsets must be multiples of 16,
+ * explicit scale offsets multiples of 4.
+ *
+ * Destination layout of an output of M x N:
+ *   FP8 : M*N code bytes, row-major, no padding inside the tensor, at
+ *         data_off; ceil(M/128) x ceil(N/128) fp32 scales, row-major,
+ *         little-endian, at scale_off. Blocks are aligned to the fused
+ *         tensor's origin; edge blocks cover only the valid elements.
+ *   BF16: M*N*2 bytes, row-major, at data_off (scale_off unused).
+ * Automatic offsets: per rank, outputs in plan order, each destination on
+ * that rank gets its data at the next 256-byte boundary, then (FP8) its
+ * scales at the next 256-byte boundary, all after the end of any
+ * explicitly placed range on that rank. */
+typedef struct {
+  const char* name;
+  int32_t num_parts;
+  const int32_t* part_params;
+  int32_t format;           /* wt_out_format */
+  int32_t num_dsts;
+  const int32_t* dst_ranks;
+  const uint64_t* dst_data_off;
+  const uint64_t* dst_scale_off;
+} wt_output_desc;
+
+/* The whole static schedule. Every param must be used by exactly one
+ * output. pool_capacity (NULL = unchecked) bounds each rank's pool size.
+ * offload_chunk_bytes > 0 enables wt_prepare_offload: the plan then owns two
+ * device staging buffers of the largest chunk's size (the GPU-memory
+ * watermark of the page's section "GPU memory usage control"). */
+typedef struct {
+  int32_t num_params;
+  const wt_param_desc* params;
+  int32_t num_outputs;
+  const wt_output_desc* outputs;
+  int32_t num_ranks;
+  const uint64_t* pool_capacity;
+  uint64_t offload_chunk_bytes;
+  uint32_t flags;
+} wt_plan_desc;
+
+typedef struct wt_plan wt_plan;
+
+/* Plan statistics (algorithmic sizes of one wt_prepare). */
+typedef struct {
+  int64_t num_units;          /* 128x128 tiles over all outputs              */
+  int64_t num_params_total;   /* elements of all params                       */
+  uint64_t bytes_read;        /* BF16 source bytes per pass                   */
+  uint64_t bytes_written;     /* destination bytes per pass (all dsts)        */
+  uint64_t host_bytes;        /* size of the packed pinned image (offload)    */
+  int32_t num_chunks;         /* offload chunks (0 if offload is disabled)    */
+  int32_t num_slots;          /* total shards = length of shard_ptrs          */
+} wt_plan_stats;
+
+/* Compile the static schedule (the page's "schedule computed once at
+ * initialization"). Validates the descriptor, resolves fusion groups and
+ * destination offsets, proves destination ranges disjoint, enumerates the
+ * 128x128 work units, and (device >= 0) uploads the tables to that device.
+ * device = -1 builds a host-only plan: layout queries work, wt_prepare*
+ * return WT_ERR_INVALID_ARGUMENT. The descriptor is deep-copied; the caller
+ * may free it on return. Errors: WT_ERR_INVALID_ARGUMENT, WT_ERR_SHAPE,
+ * WT_ERR_LAYOUT_OVERLAP, WT_ERR_POOL_TOO_SMALL, WT_ERR_ALIGNMENT,
+ * WT_ERR_OUT_OF_MEMORY, WT_ERR_CUDA. */
+wt_status wt_plan_create(const wt_plan_desc* desc, int device, wt_plan** out);
+
+/* Bytes the pool of `rank` must hold (0 for a rank with no destination). */
+wt_status wt_plan_pool_bytes(const wt_plan* p, int32_t rank, uint64_t* bytes);
+
+/* Resolved destination `dst` of output `out`. */
+wt_status wt_plan_output_layout(const wt_plan* p, int32_t out, int32_t dst,
+                                int32_t* rank, uint64_t* data_off,
+                                uint64_t* scale_off);
+
+/* Byte offset of (param, shard) inside the packed pinned-host image used
+ * by wt_prepare_offload. The image holds the params in the order their
+ * outputs appear (parts in fusion order), each param's shards in order,
+ * every shard starting at a 256-byte boundary. */
+wt_status wt_plan_shard_host_offset(const wt_plan* p, int32_t param,
+                                    int32_t shard, uint64_t* off);
+
+wt_status wt_plan_get_stats(const wt_plan* p, wt_plan_stats* stats);
+
+/* One step: run the preparation of every output on `stream`.
+ * shard_ptrs: num_slots device pointers, param-major then shard (the order
+ *   of wt_plan_desc.params and their shard_rows); each shard is a
+ *   contiguous shard_rows x cols BF16 row-major block. A shard with 0 rows
+ *   may be NULL. Shards of outputs whose cols are a multiple of 8 must be
+ *   16-byte aligned.
+ * pools: num_ranks device pointers, each 16-byte aligned, holding at least
+ *   wt_plan_pool_bytes bytes (NULL allowed for a 0-byte pool).
+ * Shards and pools are borrowed: they must stay valid until the stream
+ * work completes. Asynchronous: no allocation, no device synchronisation.
+ * The pointer tables are re-uploaded (one stream-ordered copy) only when
+ * they differ from the previous call's. Calls on one plan must be ordered
+ * on one stream (the plan holds one device pointer table).
+ * Errors: WT_ERR_INVALID_ARGUMENT (null pointer where data is needed,
+ * host-only plan), WT_ERR_ALIGNMENT, WT_ERR_CUDA (a launch or copy failed,
+ * including an earlier asynchronous error). */
+wt_status wt_prepare(wt_plan* p, const void* const* shard_ptrs,
+                     void* const* pools, void* stream);
+
+/* One step for FSDP CPU offload (the page's "host-to-device memcpy if FSDP
+ * offloads to CPU" stage, pipelined with preparation): the packed pinned
+ * host image (see wt_plan_shard_host_offset) is copied chunk by chunk into
+ * the plan's two staging buffers on copy_stream while the preparation of
+ * the previous chunk runs on compute_stream. Chunks are greedy runs of whole
+ * outputs in plan order, each at most offload_chunk_bytes of image (an
+ * output larger than that is a chunk of its own). When the call returns,
+ * all work is queued; compute_stream's completion implies the copies'.
+ * host_image must be pinned (cudaHostAlloc / cudaHostRegister) and stay
+ * untouched until then. Errors: as wt_prepare; WT_ERR_INVALID_ARGUMENT when
+ * the plan was built without offload_chunk_bytes. If queueing fails midway
+ * the call waits for what it queued and returns the error; the plan stays
+ * usable. */
+wt_status wt_prepare_offload(wt_plan* p, const void* host_image,
+                             void* const* pools, void* copy_stream,
+                             void* compute_stream);
+
+/* With WT_FLAG_DEBUG_CHECKS: synchronise `stream`, then report
+ * WT_ERR_INTERNAL if any store of an earlier wt_prepare* fell outside its
+ * destination range (the offending store is skipped, never performed), and
+ * clear the flag. Without the flag: WT_OK after the synchronisation. */
+wt_status wt_plan_check(wt_plan* p, void* stream);
+
+/* Testing hook: make chunk `chunk` of the next wt_prepare_offload calls
+ * fail on the host before it is queued (-1 disables). Exercises the
+ * drain-and-report path without touching the GPU. */
+wt_status wt_debug_fail_offload_chunk(wt_plan* p, int32_t chunk);
+
+/* Synchronise the plan's device with the last stream it ran on, then free
+ * the plan and everything it owns. NULL is accepted. */
+wt_status wt_plan_destroy(wt_plan* p);
+
+const char* wt_status_string(wt_status s);
+const char* wt_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* WT_H */
