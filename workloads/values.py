@@ -18,14 +18,18 @@ generator so they do not depend on the device):
 """
 from __future__ import annotations
 
+import zlib
+
 import numpy as np
 import torch
 
 from .configs import TILE, Workload
 
 
-def _param_seed(seed: int, p: int) -> int:
-    return (seed * 1_000_003 + p * 7919 + 17) % (2**63 - 1)
+def _param_seed(seed: int, name: str) -> int:
+    """Seed of one parameter: depends on the recipe seed and the parameter's
+    name only, so any subset of a workload draws the same values."""
+    return (seed * 1_000_003 + zlib.crc32(name.encode()) * 7919 + 17) % (2**63 - 1)
 
 
 def param_values(w: Workload, p: int, device="cpu") -> torch.Tensor:
@@ -33,7 +37,7 @@ def param_values(w: Workload, p: int, device="cpu") -> torch.Tensor:
     par = w.params[p]
     rec = w.values
     g = torch.Generator(device=device)
-    g.manual_seed(_param_seed(rec.seed, p))
+    g.manual_seed(_param_seed(rec.seed, par.name))
     shape = (par.rows, par.cols)
     if rec.dist == "normal":
         x = torch.randn(shape, generator=g, device=device, dtype=torch.float32)
@@ -60,7 +64,7 @@ def _apply_block_patterns(w: Workload, p: int, xb: torch.Tensor) -> None:
     rec = w.values
     tr, tc = -(-par.rows // TILE), -(-par.cols // TILE)
     g = torch.Generator(device="cpu")
-    g.manual_seed(_param_seed(rec.seed, p) ^ 0x5DEECE66D)
+    g.manual_seed(_param_seed(rec.seed, par.name) ^ 0x5DEECE66D)
     cat = torch.randint(0, 8, (tr, tc), generator=g)
     pos_r = torch.randint(0, TILE, (tr, tc), generator=g)
     pos_c = torch.randint(0, TILE, (tr, tc), generator=g)
