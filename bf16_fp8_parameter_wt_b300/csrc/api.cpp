@@ -43,7 +43,7 @@ void free_device(Plan& p) {
   if (p.device < 0) return;
   DeviceGuard g(p.device);
   if (p.d_tables) cudaFree(p.d_tables);
-  if (p.h_pinned_ptrs) cudaFreeHost(p.h_pinned_ptrs);
+  if (p.h_pinned) cudaFreeHost(p.h_pinned);
   for (int b = 0; b < 2; ++b) {
     if (p.staging[b]) cudaFree(p.staging[b]);
     if (p.h2d_done[b]) cudaEventDestroy(p.h2d_done[b]);
@@ -52,7 +52,22 @@ void free_device(Plan& p) {
   if (p.ptr_upload_done) cudaEventDestroy(p.ptr_upload_done);
   if (p.last_done) cudaEventDestroy(p.last_done);
   p.d_tables = nullptr;
-  p.h_pinned_ptrs = nullptr;
+  p.h_pinned = nullptr;
+}
+
+// Layout of the dynamic pointer block (identical on the device and in the
+// pinned staging buffer): shard pointers, block-row sources, destinations.
+struct DynLayout {
+  size_t shards = 0, trows = 0, dsts = 0, bytes = 0;
+};
+
+DynLayout dyn_layout(const Plan& p) {
+  DynLayout d;
+  d.shards = 0;
+  d.trows = align256(d.shards + (size_t)p.num_slots * sizeof(void*));
+  d.dsts = align256(d.trows + p.h_trows.size() * sizeof(void*));
+  d.bytes = align256(d.dsts + (size_t)p.num_dst_entries * sizeof(DevDstPtr));
+  return d;
 }
 
 // Upload the static tables and allocate what the per-step calls need, so
@@ -69,55 +84,50 @@ wt_status upload(Plan& p, int device) {
   if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
   p.grid_per_sm = prep_blocks_per_sm();
 
-  const size_t n_slots = (size_t)p.num_slots, n_ranks = (size_t)p.num_ranks;
+  const size_t n_slots = (size_t)p.num_slots, n_trows = p.h_trows.size();
   const bool offload = p.chunk_bytes > 0;
+  const DynLayout dl = dyn_layout(p);
   size_t off = 0;
   auto take = [&](size_t bytes) { size_t o = off; off = align256(off + bytes); return o; };
-  const size_t o_outs = take(p.h_outs.size() * sizeof(DevOutput));
+  const size_t o_dyn = take(dl.bytes);
+  const size_t o_units = take(p.h_units.size() * sizeof(DevUnit));
   const size_t o_runs = take(p.h_runs.size() * sizeof(DevRun));
-  const size_t o_trow = take(p.h_trow.size() * sizeof(int32_t));
-  const size_t o_dsts = take(p.h_dsts.size() * sizeof(DevDst));
-  const size_t o_unit = take(p.h_unit_out.size() * sizeof(uint32_t));
-  const size_t o_ptrs = take((n_slots + n_ranks) * sizeof(void*));   // shards, then pools
-  const size_t o_pbytes = take(n_ranks * sizeof(uint64_t));
+  const size_t o_tfr = take(p.h_trow_first_run.size() * sizeof(int32_t));
   const size_t o_err = take(sizeof(int32_t));
-  const size_t o_offl = take(offload ? n_slots * sizeof(void*) : 0);
+  const size_t o_offl_s = take(offload ? n_slots * sizeof(void*) : 0);
+  const size_t o_offl_t = take(offload ? n_trows * sizeof(void*) : 0);
   e = cudaMalloc(&p.d_tables, std::max<size_t>(off, 256));
   if (e != cudaSuccess) return fail(WT_ERR_OUT_OF_MEMORY, "cudaMalloc of plan tables failed");
   char* base = static_cast<char*>(p.d_tables);
   auto put = [&](size_t o, const void* src, size_t bytes) {
     return bytes ? cudaMemcpy(base + o, src, bytes, cudaMemcpyHostToDevice) : cudaSuccess;
   };
-  if ((e = put(o_outs, p.h_outs.data(), p.h_outs.size() * sizeof(DevOutput))) != cudaSuccess ||
+  if ((e = cudaMemset(base + o_dyn, 0, dl.bytes)) != cudaSuccess ||
+      (e = put(o_units, p.h_units.data(), p.h_units.size() * sizeof(DevUnit))) != cudaSuccess ||
       (e = put(o_runs, p.h_runs.data(), p.h_runs.size() * sizeof(DevRun))) != cudaSuccess ||
-      (e = put(o_trow, p.h_trow.data(), p.h_trow.size() * sizeof(int32_t))) != cudaSuccess ||
-      (e = put(o_dsts, p.h_dsts.data(), p.h_dsts.size() * sizeof(DevDst))) != cudaSuccess ||
-      (e = put(o_unit, p.h_unit_out.data(), p.h_unit_out.size() * sizeof(uint32_t))) != cudaSuccess ||
-      (e = put(o_pbytes, p.pool_bytes.data(), n_ranks * sizeof(uint64_t))) != cudaSuccess ||
+      (e = put(o_tfr, p.h_trow_first_run.data(), p.h_trow_first_run.size() * sizeof(int32_t))) != cudaSuccess ||
       (e = cudaMemset(base + o_err, 0, sizeof(int32_t))) != cudaSuccess)
     return cuda_fail(e, "uploading plan tables");
-  p.args.outs = reinterpret_cast<const DevOutput*>(base + o_outs);
-  p.args.runs = reinterpret_cast<const DevRun*>(base + o_runs);
-  p.args.trow_first_run = reinterpret_cast<const int32_t*>(base + o_trow);
-  p.args.dsts = reinterpret_cast<const DevDst*>(base + o_dsts);
-  p.args.unit_out = reinterpret_cast<const uint32_t*>(base + o_unit);
-  p.d_shard_ptrs = reinterpret_cast<const uint16_t**>(base + o_ptrs);
-  p.d_pool_ptrs = reinterpret_cast<uint8_t**>(base + o_ptrs + n_slots * sizeof(void*));
-  p.d_pool_bytes = reinterpret_cast<uint64_t*>(base + o_pbytes);
+  p.dyn_bytes = dl.bytes;
+  p.d_shard_ptrs = reinterpret_cast<const uint16_t**>(base + o_dyn + dl.shards);
+  p.d_trow_src = reinterpret_cast<const uint16_t**>(base + o_dyn + dl.trows);
+  p.d_dst_ptrs = reinterpret_cast<DevDstPtr*>(base + o_dyn + dl.dsts);
   p.d_error = reinterpret_cast<int32_t*>(base + o_err);
-  p.args.pool_ptrs = p.d_pool_ptrs;
-  p.args.pool_bytes = p.d_pool_bytes;
+  p.args.units = reinterpret_cast<const DevUnit*>(base + o_units);
+  p.args.runs = reinterpret_cast<const DevRun*>(base + o_runs);
+  p.args.trow_first_run = reinterpret_cast<const int32_t*>(base + o_tfr);
+  p.args.dst_ptrs = p.d_dst_ptrs;
   p.args.error_word = p.d_error;
 
-  e = cudaHostAlloc(&p.h_pinned_ptrs, std::max<size_t>((n_slots + n_ranks) * sizeof(void*), 8),
-                    cudaHostAllocDefault);
+  e = cudaHostAlloc(&p.h_pinned, std::max<size_t>(dl.bytes, 256), cudaHostAllocDefault);
   if (e != cudaSuccess) return fail(WT_ERR_OUT_OF_MEMORY, "pinned pointer staging allocation failed");
+  std::memset(p.h_pinned, 0, std::max<size_t>(dl.bytes, 256));
   if ((e = cudaEventCreateWithFlags(&p.ptr_upload_done, cudaEventDisableTiming)) != cudaSuccess ||
       (e = cudaEventCreateWithFlags(&p.last_done, cudaEventDisableTiming)) != cudaSuccess)
     return cuda_fail(e, "cudaEventCreate");
   p.cached_shards.assign(n_slots, nullptr);
-  p.cached_pools.assign(n_ranks, nullptr);
-  p.ptrs_valid = false;
+  p.cached_pools.assign((size_t)p.num_ranks, nullptr);
+  p.shards_valid = p.pools_valid = false;
 
   if (offload) {
     // the watermark: two staging buffers of the largest chunk
@@ -128,7 +138,7 @@ wt_status upload(Plan& p, int device) {
           (e = cudaEventCreateWithFlags(&p.prep_done[b], cudaEventDisableTiming)) != cudaSuccess)
         return cuda_fail(e, "cudaEventCreate");
     }
-    // static shard table: chunk c's shards live in staging[c % 2]
+    // static tables: chunk c's shards live in staging[c % 2]
     std::vector<const void*> tbl(n_slots, nullptr);
     for (size_t c = 0; c < p.chunks.size(); ++c) {
       const Chunk& ch = p.chunks[c];
@@ -142,28 +152,35 @@ wt_status upload(Plan& p, int device) {
           }
         }
     }
-    p.d_offload_shard_ptrs = reinterpret_cast<const uint16_t**>(base + o_offl);
-    if ((e = put(o_offl, tbl.data(), n_slots * sizeof(void*))) != cudaSuccess)
-      return cuda_fail(e, "uploading offload table");
+    std::vector<const uint16_t*> trs(n_trows, nullptr);
+    fill_trow_src(p, tbl.data(), trs.data());
+    p.d_offload_shard_ptrs = reinterpret_cast<const uint16_t**>(base + o_offl_s);
+    p.d_offload_trow_src = reinterpret_cast<const uint16_t**>(base + o_offl_t);
+    if ((e = put(o_offl_s, tbl.data(), n_slots * sizeof(void*))) != cudaSuccess ||
+        (e = put(o_offl_t, trs.data(), n_trows * sizeof(void*))) != cudaSuccess)
+      return cuda_fail(e, "uploading offload tables");
   }
   return WT_OK;
 }
 
-// Check the caller's pool pointers and, when they or the shard pointers
-// changed since the last call, queue one copy of the pointer table on s.
+// Check the caller's pointers and, when they changed since the last call,
+// rebuild the dynamic pointer block (shard pointers, block-row sources,
+// absolute destination addresses) on the host and queue one copy on s.
 wt_status stage_pointers(Plan& p, const void* const* shards, void* const* pools, cudaStream_t s) {
   const size_t n_slots = (size_t)p.num_slots, n_ranks = (size_t)p.num_ranks;
-  bool same = p.ptrs_valid;
-  if (same && pools) same = std::equal(p.cached_pools.begin(), p.cached_pools.end(), pools);
-  if (same && shards) same = std::equal(p.cached_shards.begin(), p.cached_shards.end(), shards);
-  if (same) return WT_OK;
-  for (size_t r = 0; r < n_ranks; ++r) {
-    if (p.pool_bytes[r] == 0) continue;
-    if (!pools[r]) return fail(WT_ERR_INVALID_ARGUMENT, "pool " + std::to_string(r) + " is NULL");
-    if (reinterpret_cast<uintptr_t>(pools[r]) % 16)
-      return fail(WT_ERR_ALIGNMENT, "pool " + std::to_string(r) + " is not 16-byte aligned");
-  }
-  if (shards) {
+  const bool shards_changed =
+      shards && !(p.shards_valid && std::equal(p.cached_shards.begin(), p.cached_shards.end(), shards));
+  const bool pools_changed =
+      !(p.pools_valid && std::equal(p.cached_pools.begin(), p.cached_pools.end(), pools));
+  if (!shards_changed && !pools_changed) return WT_OK;
+  if (pools_changed)
+    for (size_t r = 0; r < n_ranks; ++r) {
+      if (p.pool_bytes[r] == 0) continue;
+      if (!pools[r]) return fail(WT_ERR_INVALID_ARGUMENT, "pool " + std::to_string(r) + " is NULL");
+      if (reinterpret_cast<uintptr_t>(pools[r]) % 16)
+        return fail(WT_ERR_ALIGNMENT, "pool " + std::to_string(r) + " is not 16-byte aligned");
+    }
+  if (shards_changed)
     for (const ParamInfo& pi : p.params) {
       const bool vec = p.outputs[pi.output].vec;
       for (size_t k = 0; k < pi.shard_rows.size(); ++k) {
@@ -174,23 +191,37 @@ wt_status stage_pointers(Plan& p, const void* const* shards, void* const* pools,
           return fail(WT_ERR_ALIGNMENT, pi.name + ": shard " + std::to_string(k) + " is misaligned");
       }
     }
-  }
   // the pinned staging may still be read by the previous upload
   cudaError_t e = cudaEventSynchronize(p.ptr_upload_done);
   if (e != cudaSuccess) return cuda_fail(e, "waiting for the previous pointer upload");
-  const void** h = static_cast<const void**>(p.h_pinned_ptrs);
-  for (size_t i = 0; i < n_slots; ++i) h[i] = shards ? shards[i] : p.cached_shards[i];
-  for (size_t r = 0; r < n_ranks; ++r) h[n_slots + r] = pools[r];
-  if (n_slots + n_ranks) {
-    e = cudaMemcpyAsync(p.d_shard_ptrs, h, (n_slots + n_ranks) * sizeof(void*),
-                        cudaMemcpyHostToDevice, s);
-    if (e != cudaSuccess) return cuda_fail(e, "pointer table upload");
+  const DynLayout dl = dyn_layout(p);
+  char* h = static_cast<char*>(p.h_pinned);
+  if (shards_changed) {
+    std::memcpy(h + dl.shards, shards, n_slots * sizeof(void*));
+    fill_trow_src(p, shards, reinterpret_cast<const uint16_t**>(h + dl.trows));
   }
+  if (pools_changed) {
+    DevDstPtr* dp = reinterpret_cast<DevDstPtr*>(h + dl.dsts);
+    for (const OutputInfo& oi : p.outputs)
+      for (size_t k = 0; k < oi.dsts.size(); ++k) {
+        const DstInfo& ds = oi.dsts[k];
+        uint8_t* pool = static_cast<uint8_t*>(pools[ds.rank]);
+        DevDstPtr& d = dp[oi.dst_begin + k];
+        d.data = pool + ds.data_off;
+        d.scale = oi.format == WT_OUT_FP8_E4M3_B128 ? reinterpret_cast<float*>(pool + ds.scale_off) : nullptr;
+        d.pool_begin = pool;
+        d.pool_end = pool + p.pool_bytes[ds.rank];
+      }
+  }
+  e = cudaMemcpyAsync(p.d_shard_ptrs, h, dl.bytes, cudaMemcpyHostToDevice, s);
+  if (e != cudaSuccess) return cuda_fail(e, "pointer table upload");
   if ((e = cudaEventRecord(p.ptr_upload_done, s)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
-  if (shards) std::copy(shards, shards + n_slots, p.cached_shards.begin());
+  if (shards_changed) {
+    std::copy(shards, shards + n_slots, p.cached_shards.begin());
+    p.shards_valid = true;
+  }
   std::copy(pools, pools + n_ranks, p.cached_pools.begin());
-  // after an offload call the shard cache is not a valid image of the table
-  p.ptrs_valid = shards != nullptr;
+  p.pools_valid = true;
   return WT_OK;
 }
 
@@ -285,6 +316,7 @@ wt_status wt_prepare(wt_plan* h, const void* const* shard_ptrs, void* const* poo
   if (st != WT_OK) return st;
   PrepArgs a = p.args;
   a.shard_ptrs = p.d_shard_ptrs;
+  a.trow_src = p.d_trow_src;
   a.unit_begin = 0;
   a.unit_end = p.num_units;
   cudaError_t e = launch_prepare(a, grid_for(p, p.num_units), s, p.flags & WT_FLAG_DEBUG_CHECKS);
@@ -310,6 +342,7 @@ wt_status wt_prepare_offload(wt_plan* h, const void* host_image, void* const* po
   if (st != WT_OK) return st;
   PrepArgs a = p.args;
   a.shard_ptrs = p.d_offload_shard_ptrs;
+  a.trow_src = p.d_offload_trow_src;
   const char* host = static_cast<const char*>(host_image);
   auto drain = [&](wt_status s_, const std::string& msg) {
     cudaStreamSynchronize(cs);

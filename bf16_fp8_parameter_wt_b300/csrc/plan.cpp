@@ -38,7 +38,7 @@ struct Range {
 }  // namespace
 
 wt_status compile_plan(const wt_plan_desc* d, Plan* p) {
-  const int64_t kMaxDim = int64_t(1) << 40;
+  const int64_t kMaxDim = (int64_t(1) << 31) - 1;
   if (!d) return fail(WT_ERR_INVALID_ARGUMENT, "descriptor is NULL");
   if (d->num_params < 0 || d->num_outputs < 0 || d->num_ranks < 0)
     return fail(WT_ERR_INVALID_ARGUMENT, "negative count in descriptor");
@@ -205,27 +205,19 @@ wt_status compile_plan(const wt_plan_desc* d, Plan* p) {
                                              std::to_string(p->pool_bytes[r]) + " bytes");
   }
 
-  // ---- device tables: outputs, row runs, tile rows, destinations, units ---
-  p->h_outs.clear();
+  // ---- device tables: units, row runs, block rows ------------------------
+  p->h_units.clear();
   p->h_runs.clear();
-  p->h_trow.clear();
-  p->h_dsts.clear();
-  p->h_unit_out.assign((size_t)units, 0);
+  p->h_trows.clear();
+  p->h_trow_first_run.clear();
+  p->h_units.reserve((size_t)units);
+  int32_t dst_entries = 0;
   for (int o = 0; o < (int)p->outputs.size(); ++o) {
     auto& oi = p->outputs[o];
-    DevOutput dv{};
-    dv.rows = oi.rows;
-    dv.cols = oi.cols;
-    dv.unit_begin = oi.unit_begin;
-    dv.tiles_n = (int32_t)ceil_div(oi.cols, kTile);
-    dv.fp8 = oi.format == WT_OUT_FP8_E4M3_B128;
-    dv.vec = oi.vec;
-    dv.num_dsts = (int32_t)oi.dsts.size();
-    dv.dst_begin = (int32_t)p->h_dsts.size();
-    dv.trow_begin = (int32_t)p->h_trow.size();
-    for (auto& ds : oi.dsts) p->h_dsts.push_back({ds.rank, 0, ds.data_off, ds.scale_off});
+    oi.dst_begin = dst_entries;
+    dst_entries += (int32_t)oi.dsts.size();
     // the runs of this output: shards of its parts in fusion order, empty
-    // shards skipped (reassembly = row r of the part comes from the shard
+    // shards skipped (reassembly: row r of the part comes from the shard
     // whose row range holds r)
     const size_t first_run = p->h_runs.size();
     int64_t row = 0;
@@ -237,14 +229,39 @@ wt_status compile_plan(const wt_plan_desc* d, Plan* p) {
         row += pi.shard_rows[s];
       }
     }
+    const int64_t tiles_n = ceil_div(oi.cols, kTile);
+    const uint32_t flags = (oi.format == WT_OUT_FP8_E4M3_B128 ? kUnitFp8 : 0u) |
+                           (oi.vec ? kUnitVec : 0u);
     size_t k = first_run;
     for (int64_t bi = 0; bi * kTile < oi.rows; ++bi) {
-      while (p->h_runs[k].row0 + p->h_runs[k].rows <= bi * kTile) ++k;
-      p->h_trow.push_back((int32_t)k);
+      const int64_t r0 = bi * kTile;
+      const int64_t nrows = std::min<int64_t>(kTile, oi.rows - r0);
+      while (p->h_runs[k].row0 + p->h_runs[k].rows <= r0) ++k;
+      TileRowInfo tr;
+      tr.output = o;
+      tr.first_run = (int32_t)k;
+      tr.single = p->h_runs[k].row0 + p->h_runs[k].rows >= r0 + nrows;
+      tr.row_in_run = r0 - p->h_runs[k].row0;
+      const uint32_t gtr = (uint32_t)p->h_trows.size();
+      p->h_trows.push_back(tr);
+      p->h_trow_first_run.push_back((int32_t)k);
+      const uint32_t f = flags | (tr.single ? 0u : kUnitMulti);
+      for (int64_t bj = 0; bj < tiles_n; ++bj) {
+        const int64_t ncols = std::min<int64_t>(kTile, oi.cols - bj * kTile);
+        DevUnit u;
+        u.o = (uint32_t)o;
+        u.gtr = gtr;
+        u.bi = (uint32_t)bi;
+        u.bj = (uint32_t)bj;
+        u.cols = (uint32_t)oi.cols;
+        u.shape = (uint32_t)(nrows - 1) | ((uint32_t)(ncols - 1) << 8) | (f << 16);
+        u.num_dsts = (uint32_t)oi.dsts.size();
+        u.dst_begin = (uint32_t)oi.dst_begin;
+        p->h_units.push_back(u);
+      }
     }
-    for (int64_t u = 0; u < oi.num_units; ++u) p->h_unit_out[oi.unit_begin + u] = (uint32_t)o;
-    p->h_outs.push_back(dv);
   }
+  p->num_dst_entries = dst_entries;
 
   // ---- packed host image for offload and its chunks ----------------------
   p->shard_host_off.assign(p->num_slots, 0);
@@ -287,6 +304,19 @@ wt_status compile_plan(const wt_plan_desc* d, Plan* p) {
     }
   }
   return WT_OK;
+}
+
+void fill_trow_src(const Plan& p, const void* const* shards, const uint16_t** out) {
+  for (size_t g = 0; g < p.h_trows.size(); ++g) {
+    const TileRowInfo& tr = p.h_trows[g];
+    if (!tr.single) {
+      out[g] = nullptr;
+      continue;
+    }
+    const DevRun& run = p.h_runs[tr.first_run];
+    const uint16_t* base = static_cast<const uint16_t*>(shards[run.slot]);
+    out[g] = base + tr.row_in_run * p.outputs[tr.output].cols;
+  }
 }
 
 }  // namespace wt

@@ -17,18 +17,23 @@ namespace wt {
 constexpr int kTile = 128;        // block edge (rows and cols)
 constexpr int kThreads = 256;     // threads per CTA of the preparation kernel
 
-// One output tensor (device table entry).
-struct DevOutput {
-  int64_t rows, cols;      // M x N of the fused tensor
-  int64_t unit_begin;      // global index of its first 128x128 unit
-  int32_t tiles_n;         // ceil(N / 128)
-  int32_t fp8;             // 1: e4m3 codes + scales, 0: BF16 bytes
-  int32_t vec;             // 1: 16-byte vector path, 0: element path
-  int32_t num_dsts;
-  int32_t dst_begin;       // first entry in the DevDst table
-  int32_t trow_begin;      // first entry in the tile-row table
+// DevUnit.shape flag bits (bits 16..23)
+constexpr uint32_t kUnitFp8 = 1u;    // e4m3 codes + scale, else BF16 bytes
+constexpr uint32_t kUnitVec = 2u;    // 16-byte vector path, else element path
+constexpr uint32_t kUnitMulti = 4u;  // block rows come from more than one shard
+
+// Static descriptor of one 128x128 work unit, 32 bytes (eight words that
+// one warp fetches with one coalesced load).
+struct DevUnit {
+  uint32_t o;          // output index
+  uint32_t gtr;        // global block-row index (source pointer tables)
+  uint32_t bi, bj;     // block row / column inside the output
+  uint32_t cols;       // N: elements per row of the output
+  uint32_t shape;      // (nrows - 1) | (ncols - 1) << 8 | flags << 16
+  uint32_t num_dsts;
+  uint32_t dst_begin;  // first entry of the destination pointer table
 };
-static_assert(sizeof(DevOutput) == 48, "layout");
+static_assert(sizeof(DevUnit) == 32, "layout");
 
 // A run of consecutive fused rows that come from one shard.
 struct DevRun {
@@ -39,27 +44,26 @@ struct DevRun {
 };
 static_assert(sizeof(DevRun) == 24, "layout");
 
-// One destination of one output.
-struct DevDst {
-  int32_t rank;
-  int32_t pad;
-  uint64_t data_off;
-  uint64_t scale_off;
+// Absolute addresses of one (output, destination), rebuilt on the host
+// whenever the caller's pools change.
+struct DevDstPtr {
+  uint8_t* data;
+  float* scale;
+  const uint8_t* pool_begin;   // for the debug bounds check
+  const uint8_t* pool_end;
 };
-static_assert(sizeof(DevDst) == 24, "layout");
+static_assert(sizeof(DevDstPtr) == 32, "layout");
 
 // Everything one launch of the preparation kernel reads.
 struct PrepArgs {
-  const DevOutput* outs;
+  const DevUnit* units;
+  const uint16_t* const* trow_src;   // per block row: address of its first row (one-shard rows)
+  const int32_t* trow_first_run;     // per block row: first run touching it (multi-shard rows)
   const DevRun* runs;
-  const int32_t* trow_first_run;   // per tile row: first run that touches it
-  const DevDst* dsts;
-  const uint32_t* unit_out;        // per unit: its output
   const uint16_t* const* shard_ptrs;
-  uint8_t* const* pool_ptrs;
-  const uint64_t* pool_bytes;
+  const DevDstPtr* dst_ptrs;
   int64_t unit_begin, unit_end;
-  int32_t* error_word;             // debug checks: set to 1 on a bad store
+  int32_t* error_word;               // debug checks: set to 1 on a bad store
 };
 
 // Host-side copy of one param.
@@ -84,7 +88,16 @@ struct OutputInfo {
   std::vector<DstInfo> dsts;
   uint64_t data_bytes = 0, scale_bytes = 0;
   int64_t unit_begin = 0, num_units = 0;
+  int32_t dst_begin = 0;    // first entry of the destination pointer table
   bool vec = false;
+};
+
+// Host view of one block row, used to rebuild its source address.
+struct TileRowInfo {
+  int32_t output = 0;
+  int32_t first_run = 0;    // index into runs
+  bool single = true;       // all of its rows come from runs[first_run]
+  int64_t row_in_run = 0;   // first row of the block row, relative to the run
 };
 
 // An offload chunk: a run of whole outputs, contiguous in the host image.
@@ -105,33 +118,35 @@ struct Plan {
   std::vector<uint64_t> shard_host_off;   // per slot
   uint64_t host_bytes = 0;
   int32_t num_slots = 0;
+  int32_t num_dst_entries = 0;
   int64_t num_units = 0;
   uint64_t bytes_read = 0, bytes_written = 0;
   int64_t num_params_total = 0;
 
-  // host images of the device tables
-  std::vector<DevOutput> h_outs;
+  // host images of the static device tables
+  std::vector<DevUnit> h_units;
   std::vector<DevRun> h_runs;
-  std::vector<int32_t> h_trow;
-  std::vector<DevDst> h_dsts;
-  std::vector<uint32_t> h_unit_out;
+  std::vector<TileRowInfo> h_trows;
+  std::vector<int32_t> h_trow_first_run;
 
-  // device side
-  void* d_tables = nullptr;          // one allocation for all static tables
-  PrepArgs args{};                   // pointers into d_tables
-  const uint16_t** d_shard_ptrs = nullptr;
-  uint8_t** d_pool_ptrs = nullptr;
-  uint64_t* d_pool_bytes = nullptr;
+  // device side: one allocation for the static tables, one for the
+  // pointer tables that follow the caller's buffers
+  void* d_tables = nullptr;
+  PrepArgs args{};                   // static parts filled at upload
+  const uint16_t** d_shard_ptrs = nullptr;      // dynamic block: shard ptrs,
+  const uint16_t** d_trow_src = nullptr;        //   block-row sources,
+  DevDstPtr* d_dst_ptrs = nullptr;              //   destination pointers
+  size_t dyn_bytes = 0;                         // size of that block
   int32_t* d_error = nullptr;
-  void* h_pinned_ptrs = nullptr;     // pinned staging for pointer uploads
+  void* h_pinned = nullptr;          // pinned staging of the dynamic block
   std::vector<const void*> cached_shards;
   std::vector<void*> cached_pools;
-  bool ptrs_valid = false;
+  bool shards_valid = false, pools_valid = false;
   cudaEvent_t ptr_upload_done = nullptr;
   cudaEvent_t last_done = nullptr;
   bool ran = false;
   int sm_count = 0;
-  int grid_per_sm = 4;
+  int grid_per_sm = 3;
 
   // offload
   uint64_t chunk_bytes = 0;
@@ -139,6 +154,7 @@ struct Plan {
   uint64_t staging_bytes = 0;
   void* staging[2] = {nullptr, nullptr};
   const uint16_t** d_offload_shard_ptrs = nullptr;
+  const uint16_t** d_offload_trow_src = nullptr;
   cudaEvent_t h2d_done[2] = {nullptr, nullptr};
   cudaEvent_t prep_done[2] = {nullptr, nullptr};
   bool prep_recorded[2] = {false, false};
@@ -147,6 +163,8 @@ struct Plan {
 
 // plan.cpp
 wt_status compile_plan(const wt_plan_desc* d, Plan* p);   // host only
+// Source address of every block row, given the shard address of every slot.
+void fill_trow_src(const Plan& p, const void* const* shards, const uint16_t** out);
 void set_error(const std::string& msg);
 
 // prep_kernel.cu
