@@ -1,0 +1,159 @@
+// wt_prepare_noalloc: one preparation step that allocates no device memory.
+//
+// wt_plan_create keeps its schedule tables (unit descriptors, row runs,
+// pointer tables, an error word) in device memory it obtains with
+// cudaMalloc. Some callers cannot allow that: code that runs inside a
+// memory pool or arena it does not own, a process whose device memory is
+// fully reserved up front by an inference engine, or a host path that must
+// not touch the device allocator at all. For them this entry point compiles
+// the schedule on the host on every call and copies its tables into one
+// fixed scratch array that lives in the library image on each device, then
+// runs the same preparation kernel as wt_prepare. The caller passes inputs
+// (shards) and outputs (pools) as usual.
+#include <algorithm>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "plan.h"
+
+namespace wt {
+namespace {
+
+// Maximum size of the schedule tables one call may use. Every device that
+// loads the library holds this array until the process exits.
+constexpr size_t kNoAllocScratchBytes = size_t(4) << 20;   // 4 MiB
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+void* g_scratch_addr[kMaxDevices] = {};   // device address of the array, per device
+int g_sm_count[kMaxDevices] = {};
+int g_blocks_per_sm[kMaxDevices] = {};
+
+size_t up256(size_t v) { return (v + 255) & ~size_t(255); }
+
+wt_status fail_na(wt_status s, const std::string& msg) {
+  set_error(msg);
+  return s;
+}
+
+// With `device` current: the array's device address (host code only sees a
+// host-side stand-in under its name) and the launch geometry, once per device.
+wt_status device_setup(int device) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (g_scratch_addr[device]) return WT_OK;
+  void* ptr = nullptr;
+  cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+  if (e != cudaSuccess || !ptr)
+    return fail_na(WT_ERR_CUDA, std::string("cudaGetSymbolAddress of the scratch array: ") +
+                                    cudaGetErrorString(e));
+  int sms = 0;
+  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
+  if (e != cudaSuccess) return fail_na(WT_ERR_CUDA, std::string("cudaDeviceGetAttribute: ") + cudaGetErrorString(e));
+  g_sm_count[device] = sms;
+  g_blocks_per_sm[device] = prep_blocks_per_sm();
+  g_scratch_addr[device] = ptr;
+  return WT_OK;
+}
+
+}  // namespace
+}  // namespace wt
+
+using namespace wt;
+
+extern "C" wt_status wt_prepare_noalloc(const wt_plan_desc* desc, const void* const* shard_ptrs,
+                                        void* const* pools, void* stream) {
+  if (!desc) return fail_na(WT_ERR_INVALID_ARGUMENT, "descriptor is NULL");
+  if (desc->offload_chunk_bytes != 0)
+    return fail_na(WT_ERR_INVALID_ARGUMENT, "wt_prepare_noalloc does not stage offloaded shards");
+  if (desc->flags & WT_FLAG_DEBUG_CHECKS)
+    return fail_na(WT_ERR_INVALID_ARGUMENT, "wt_prepare_noalloc has no debug-check readback");
+  Plan p;
+  wt_status st = compile_plan(desc, &p);
+  if (st != WT_OK) return st;
+
+  // table image: shard pointers, block-row sources, destinations, unit
+  // descriptors, runs, first run per block row, error word
+  const size_t n_slots = (size_t)p.num_slots, n_trows = p.h_trows.size();
+  const size_t o_shards = 0;
+  const size_t o_trows = up256(o_shards + n_slots * sizeof(void*));
+  const size_t o_dsts = up256(o_trows + n_trows * sizeof(void*));
+  const size_t o_units = up256(o_dsts + (size_t)p.num_dst_entries * sizeof(DevDstPtr));
+  const size_t o_runs = up256(o_units + p.h_units.size() * sizeof(DevUnit));
+  const size_t o_tfr = up256(o_runs + p.h_runs.size() * sizeof(DevRun));
+  const size_t o_err = up256(o_tfr + n_trows * sizeof(int32_t));
+  const size_t total = o_err + 256;
+  if (total > kNoAllocScratchBytes)
+    return fail_na(WT_ERR_INVALID_ARGUMENT,
+                   "schedule tables need " + std::to_string(total) +
+                       " bytes; wt_prepare_noalloc holds at most " +
+                       std::to_string(kNoAllocScratchBytes) + " bytes (use wt_plan_create)");
+  if ((n_slots > 0 && !shard_ptrs) || (p.num_ranks > 0 && !pools))
+    return fail_na(WT_ERR_INVALID_ARGUMENT, "shard_ptrs or pools is NULL");
+  for (int32_t r = 0; r < p.num_ranks; ++r) {
+    if (p.pool_bytes[r] == 0) continue;
+    if (!pools[r]) return fail_na(WT_ERR_INVALID_ARGUMENT, "pool " + std::to_string(r) + " is NULL");
+    if (reinterpret_cast<uintptr_t>(pools[r]) % 16)
+      return fail_na(WT_ERR_ALIGNMENT, "pool " + std::to_string(r) + " is not 16-byte aligned");
+  }
+  for (const ParamInfo& pi : p.params) {
+    const bool vec = p.outputs[pi.output].vec;
+    for (size_t k = 0; k < pi.shard_rows.size(); ++k) {
+      const void* ptr = shard_ptrs[pi.slot_base + k];
+      if (pi.shard_rows[k] == 0) continue;
+      if (!ptr) return fail_na(WT_ERR_INVALID_ARGUMENT, pi.name + ": shard " + std::to_string(k) + " is NULL");
+      if (reinterpret_cast<uintptr_t>(ptr) % (vec ? 16 : 2))
+        return fail_na(WT_ERR_ALIGNMENT, pi.name + ": shard " + std::to_string(k) + " is misaligned");
+    }
+  }
+
+  int device = -1;
+  cudaError_t e = cudaGetDevice(&device);
+  if (e != cudaSuccess) return fail_na(WT_ERR_CUDA, std::string("cudaGetDevice: ") + cudaGetErrorString(e));
+  if (device < 0 || device >= kMaxDevices) return fail_na(WT_ERR_INVALID_ARGUMENT, "device index out of range");
+  if ((st = device_setup(device)) != WT_OK) return st;
+  char* dbase = static_cast<char*>(g_scratch_addr[device]);
+
+  std::vector<unsigned char> img(total, 0);   // host image; the error word starts at zero
+  unsigned char* h = img.data();
+  if (n_slots) std::memcpy(h + o_shards, shard_ptrs, n_slots * sizeof(void*));
+  fill_trow_src(p, shard_ptrs, reinterpret_cast<const uint16_t**>(h + o_trows));
+  DevDstPtr* dp = reinterpret_cast<DevDstPtr*>(h + o_dsts);
+  for (const OutputInfo& oi : p.outputs)
+    for (size_t k = 0; k < oi.dsts.size(); ++k) {
+      const DstInfo& ds = oi.dsts[k];
+      uint8_t* pool = static_cast<uint8_t*>(pools[ds.rank]);
+      DevDstPtr& d = dp[oi.dst_begin + k];
+      d.data = pool + ds.data_off;
+      d.scale = oi.format == WT_OUT_FP8_E4M3_B128 ? reinterpret_cast<float*>(pool + ds.scale_off) : nullptr;
+      d.pool_begin = pool;
+      d.pool_end = pool + p.pool_bytes[ds.rank];
+    }
+  if (!p.h_units.empty()) std::memcpy(h + o_units, p.h_units.data(), p.h_units.size() * sizeof(DevUnit));
+  if (!p.h_runs.empty()) std::memcpy(h + o_runs, p.h_runs.data(), p.h_runs.size() * sizeof(DevRun));
+  if (!p.h_trow_first_run.empty())
+    std::memcpy(h + o_tfr, p.h_trow_first_run.data(), p.h_trow_first_run.size() * sizeof(int32_t));
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // from pageable memory: the call returns once the image has been staged
+  e = cudaMemcpyAsync(dbase, h, total, cudaMemcpyHostToDevice, s);
+  if (e != cudaSuccess) return fail_na(WT_ERR_CUDA, std::string("scratch upload: ") + cudaGetErrorString(e));
+
+  PrepArgs a{};
+  a.units = reinterpret_cast<const DevUnit*>(dbase + o_units);
+  a.trow_src = reinterpret_cast<const uint16_t* const*>(dbase + o_trows);
+  a.trow_first_run = reinterpret_cast<const int32_t*>(dbase + o_tfr);
+  a.runs = reinterpret_cast<const DevRun*>(dbase + o_runs);
+  a.shard_ptrs = reinterpret_cast<const uint16_t* const*>(dbase + o_shards);
+  a.dst_ptrs = reinterpret_cast<const DevDstPtr*>(dbase + o_dsts);
+  a.unit_begin = 0;
+  a.unit_end = p.num_units;
+  a.error_word = reinterpret_cast<int32_t*>(dbase + o_err);
+  const int64_t full = (int64_t)g_sm_count[device] * g_blocks_per_sm[device];
+  const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(p.num_units, full));
+  e = launch_prepare(a, grid, s, false);
+  if (e != cudaSuccess) return fail_na(WT_ERR_CUDA, std::string("preparation kernel launch: ") + cudaGetErrorString(e));
+  return WT_OK;
+}

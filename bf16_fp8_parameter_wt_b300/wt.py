@@ -27,7 +27,7 @@ WT_FLAG_DEBUG_CHECKS = 0x2
 # every entry point include/wt.h declares
 EXPORTS = ["wt_plan_create", "wt_plan_pool_bytes", "wt_plan_output_layout",
            "wt_plan_shard_host_offset", "wt_plan_get_stats", "wt_prepare", "wt_prepare_offload",
-           "wt_plan_check", "wt_debug_fail_offload_chunk", "wt_plan_destroy",
+           "wt_plan_check", "wt_debug_fail_offload_chunk", "wt_plan_destroy", "wt_prepare_noalloc",
            "wt_status_string", "wt_last_error"]
 
 
@@ -83,6 +83,7 @@ def lib() -> C.CDLL:
         L.wt_plan_get_stats.argtypes = [P, C.POINTER(wt_plan_stats)]
         L.wt_prepare.argtypes = [P, P, P, P]
         L.wt_prepare_offload.argtypes = [P, P, P, P, P]
+        L.wt_prepare_noalloc.argtypes = [C.POINTER(wt_plan_desc), P, P, P]
         L.wt_plan_check.argtypes = [P, P]
         L.wt_debug_fail_offload_chunk.argtypes = [P, C.c_int32]
         L.wt_plan_destroy.argtypes = [P]
@@ -190,6 +191,15 @@ def wt_prepare_offload(plan: int, host_image: int, pools: Sequence[int], copy_st
                        compute_stream: int) -> None:
     _check(lib().wt_prepare_offload(plan, host_image or None, _ptr_array(pools),
                                     copy_stream or None, compute_stream or None))
+
+
+def wt_prepare_noalloc(desc: "PlanDesc", shard_ptrs: Sequence[int], pools: Sequence[int],
+                       stream: int = 0) -> None:
+    """One step without any device allocation (see include/wt.h): the
+    schedule of `desc` is rebuilt on every call into the library's fixed
+    scratch array. Calls overlapping on the GPU share that array and race."""
+    _check(lib().wt_prepare_noalloc(C.byref(desc.c), _ptr_array(shard_ptrs), _ptr_array(pools),
+                                    stream or None))
 
 
 def wt_plan_check(plan: int, stream: int = 0) -> None:

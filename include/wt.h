@@ -198,6 +198,25 @@ wt_status wt_prepare_offload(wt_plan* p, const void* host_image,
                              void* const* pools, void* copy_stream,
                              void* compute_stream);
 
+/* One step that allocates no device memory. The pages have no counterpart:
+ * this exists for callers that cannot call cudaMalloc -- code running
+ * inside a memory pool or arena it does not own, or next to an engine that
+ * has reserved all device memory up front. Instead of a plan's cudaMalloc'd
+ * tables, every call compiles `desc` on the host and copies its schedule
+ * tables into one fixed 4 MiB array inside the library image (each device
+ * that loads the library holds it until the process exits), then runs the
+ * same kernel as wt_prepare on the current device. Arguments and results
+ * are those of wt_plan_create(desc) + wt_prepare(shard_ptrs, pools, stream).
+ * The first call on a device looks up the array's device address there;
+ * make that first call before any stream capture. Every call shares the
+ * array, so calls whose work overlaps on the GPU (other streams, or other
+ * threads) race: order them on one stream. Errors: as wt_plan_create and
+ * wt_prepare; WT_ERR_INVALID_ARGUMENT when the tables need more than the
+ * array's 4 MiB (roughly 120k 128x128 blocks), when offload_chunk_bytes is
+ * set, or with WT_FLAG_DEBUG_CHECKS. Never calls cudaMalloc or cudaFree. */
+wt_status wt_prepare_noalloc(const wt_plan_desc* desc, const void* const* shard_ptrs,
+                             void* const* pools, void* stream);
+
 /* With WT_FLAG_DEBUG_CHECKS: synchronise `stream`, then report
  * WT_ERR_INTERNAL if any store of an earlier wt_prepare* fell outside its
  * destination range (the offending store is skipped, never performed), and

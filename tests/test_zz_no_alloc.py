@@ -1,0 +1,88 @@
+"""wt_prepare_noalloc against wt_prepare.
+
+wt_prepare_noalloc is for callers that cannot let a library call cudaMalloc
+(code running inside a memory pool it does not own, or beside an engine that
+has reserved all device memory): it keeps its schedule tables in a fixed
+array inside the library instead. Its results must be the bytes wt_prepare
+writes, bit for bit (the tolerance of every parity test here), on two calls
+in a row -- the second call reuses the array the first one left behind.
+This file is collected last so that a run stopping at the first failure has
+already run every other test; it also passes alone in a fresh process.
+"""
+import numpy as np
+import pytest
+import torch
+
+import bf16_fp8_parameter_wt_b300 as wt
+from workloads import Output, Param, ValueRecipe, Workload, kimi_k2_moe_layer, make_shards, tiny_dense
+
+pytestmark = pytest.mark.gpu
+
+CANARY = 0xA5
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from bf16_fp8_parameter_wt_b300 import build
+    build.build()
+    assert torch.cuda.is_available()
+
+
+def _pools(plan, num_ranks, fill):
+    return [torch.full((max(1, plan.pool_bytes(r)) + 256,), fill, dtype=torch.uint8, device="cuda:0")
+            for r in range(num_ranks)]
+
+
+def _small_shapes():
+    # ragged edges, a 2050-column element-path output, multi-shard block rows,
+    # an empty shard, BF16 pass-through and a replicated destination
+    params = [Param("a", 300, 264, (1,) * 44 + (256,)), Param("b", 3, 2050, (2, 0, 1)),
+              Param("c1", 50, 130, (17, 33)), Param("c2", 79, 130, (1, 0, 40, 38)),
+              Param("n", 256, 1, (100, 100, 56))]
+    outs = [Output("a", (0,), True, (0, 1)), Output("b", (1,), True, (1,)),
+            Output("c", (2, 3), True, (0,)), Output("n", (4,), False, (1,))]
+    return Workload("noalloc_small", params, outs, 2, ValueRecipe("student_t3", 0.02, 31))
+
+
+@pytest.mark.parametrize("make", [tiny_dense, _small_shapes])
+def test_noalloc_matches_prepare_on_two_calls(make):
+    w = make()
+    shards = make_shards(w, device="cuda:0")
+    flat = [s.data_ptr() if s.numel() else 0 for per in shards for s in per]
+    stream = torch.cuda.current_stream().cuda_stream
+    plan = wt.Plan(w, device=0)
+    want = _pools(plan, w.num_ranks, CANARY)
+    plan.prepare(flat, [p.data_ptr() for p in want], stream)
+    torch.cuda.synchronize()
+    want_host = [p.cpu().numpy() for p in want]
+    # which pool bytes the schedule writes (the rest is alignment padding)
+    masks = [np.zeros(plan.pool_bytes(r) + 256, bool) for r in range(w.num_ranks)]
+    for o, out in enumerate(w.outputs):
+        m_, n_ = w.output_shape(o)
+        data = m_ * n_ * (1 if out.fp8 else 2)
+        scales = 4 * (-(-m_ // 128)) * (-(-n_ // 128)) if out.fp8 else 0
+        for k in range(len(out.dst_ranks)):
+            rank, doff, soff = plan.output_layout(o, k)
+            masks[rank][doff:doff + data] = True
+            masks[rank][soff:soff + scales] = True
+    desc = wt.PlanDesc(w)
+    for call in range(2):
+        # a different fill each call: every scheduled byte must be rewritten,
+        # and nothing else may be touched
+        fill = CANARY if call == 0 else 0x5A
+        got = _pools(plan, w.num_ranks, fill)
+        wt.wt_prepare_noalloc(desc, flat, [p.data_ptr() for p in got], stream)
+        torch.cuda.synchronize()
+        for r in range(w.num_ranks):
+            g = got[r].cpu().numpy()
+            assert np.array_equal(g[masks[r]], want_host[r][masks[r]]), (call, r)
+            assert np.all(g[~masks[r]] == fill), (call, r)
+    plan.close()
+
+
+def test_noalloc_rejects_schedules_beyond_its_array():
+    w = kimi_k2_moe_layer()          # about a million blocks: 33 MB of tables
+    with pytest.raises(wt.WTError) as ei:
+        wt.wt_prepare_noalloc(wt.PlanDesc(w), [], [0] * w.num_ranks)
+    assert ei.value.name == "WT_ERR_INVALID_ARGUMENT"
+    assert "at most" in str(ei.value)
