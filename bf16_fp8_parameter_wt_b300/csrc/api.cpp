@@ -56,16 +56,16 @@ void free_device(Plan& p) {
 }
 
 // Layout of the dynamic pointer block (identical on the device and in the
-// pinned staging buffer): shard pointers, block-row sources, destinations.
+// pinned staging buffer): shard pointers, their tensor maps, destinations.
 struct DynLayout {
-  size_t shards = 0, trows = 0, dsts = 0, bytes = 0;
+  size_t shards = 0, tmaps = 0, dsts = 0, bytes = 0;
 };
 
 DynLayout dyn_layout(const Plan& p) {
   DynLayout d;
   d.shards = 0;
-  d.trows = align256(d.shards + (size_t)p.num_slots * sizeof(void*));
-  d.dsts = align256(d.trows + p.h_trows.size() * sizeof(void*));
+  d.tmaps = align256(d.shards + (size_t)p.num_slots * sizeof(void*));
+  d.dsts = align256(d.tmaps + (size_t)p.num_slots * kTmapBytes);
   d.bytes = align256(d.dsts + (size_t)p.num_dst_entries * sizeof(DevDstPtr));
   return d;
 }
@@ -82,9 +82,9 @@ wt_status upload(Plan& p, int device) {
   p.device = device;
   e = cudaDeviceGetAttribute(&p.sm_count, cudaDevAttrMultiProcessorCount, device);
   if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
-  p.grid_per_sm = prep_blocks_per_sm();
+  if ((e = prep_kernel_setup()) != cudaSuccess) return cuda_fail(e, "preparation kernel set-up");
 
-  const size_t n_slots = (size_t)p.num_slots, n_trows = p.h_trows.size();
+  const size_t n_slots = (size_t)p.num_slots;
   const bool offload = p.chunk_bytes > 0;
   const DynLayout dl = dyn_layout(p);
   size_t off = 0;
@@ -92,10 +92,9 @@ wt_status upload(Plan& p, int device) {
   const size_t o_dyn = take(dl.bytes);
   const size_t o_units = take(p.h_units.size() * sizeof(DevUnit));
   const size_t o_runs = take(p.h_runs.size() * sizeof(DevRun));
-  const size_t o_tfr = take(p.h_trow_first_run.size() * sizeof(int32_t));
   const size_t o_err = take(sizeof(int32_t));
   const size_t o_offl_s = take(offload ? n_slots * sizeof(void*) : 0);
-  const size_t o_offl_t = take(offload ? n_trows * sizeof(void*) : 0);
+  const size_t o_offl_t = take(offload ? n_slots * kTmapBytes : 0);
   e = cudaMalloc(&p.d_tables, std::max<size_t>(off, 256));
   if (e != cudaSuccess) return fail(WT_ERR_OUT_OF_MEMORY, "cudaMalloc of plan tables failed");
   char* base = static_cast<char*>(p.d_tables);
@@ -105,19 +104,18 @@ wt_status upload(Plan& p, int device) {
   if ((e = cudaMemset(base + o_dyn, 0, dl.bytes)) != cudaSuccess ||
       (e = put(o_units, p.h_units.data(), p.h_units.size() * sizeof(DevUnit))) != cudaSuccess ||
       (e = put(o_runs, p.h_runs.data(), p.h_runs.size() * sizeof(DevRun))) != cudaSuccess ||
-      (e = put(o_tfr, p.h_trow_first_run.data(), p.h_trow_first_run.size() * sizeof(int32_t))) != cudaSuccess ||
       (e = cudaMemset(base + o_err, 0, sizeof(int32_t))) != cudaSuccess)
     return cuda_fail(e, "uploading plan tables");
   p.dyn_bytes = dl.bytes;
   p.d_shard_ptrs = reinterpret_cast<const uint16_t**>(base + o_dyn + dl.shards);
-  p.d_trow_src = reinterpret_cast<const uint16_t**>(base + o_dyn + dl.trows);
+  p.d_tmaps = reinterpret_cast<unsigned char*>(base + o_dyn + dl.tmaps);
   p.d_dst_ptrs = reinterpret_cast<DevDstPtr*>(base + o_dyn + dl.dsts);
   p.d_error = reinterpret_cast<int32_t*>(base + o_err);
   p.args.units = reinterpret_cast<const DevUnit*>(base + o_units);
   p.args.runs = reinterpret_cast<const DevRun*>(base + o_runs);
-  p.args.trow_first_run = reinterpret_cast<const int32_t*>(base + o_tfr);
   p.args.dst_ptrs = p.d_dst_ptrs;
   p.args.error_word = p.d_error;
+  p.args.timeout_ns = kDefaultTimeoutNs;
 
   e = cudaHostAlloc(&p.h_pinned, std::max<size_t>(dl.bytes, 256), cudaHostAllocDefault);
   if (e != cudaSuccess) return fail(WT_ERR_OUT_OF_MEMORY, "pinned pointer staging allocation failed");
@@ -152,20 +150,24 @@ wt_status upload(Plan& p, int device) {
           }
         }
     }
-    std::vector<const uint16_t*> trs(n_trows, nullptr);
-    fill_trow_src(p, tbl.data(), trs.data());
+    std::vector<unsigned char> maps(n_slots * kTmapBytes);
+    if (n_slots) {
+      wt_status st = encode_tmaps(p, tbl.data(), maps.data());
+      if (st != WT_OK) return st;
+    }
     p.d_offload_shard_ptrs = reinterpret_cast<const uint16_t**>(base + o_offl_s);
-    p.d_offload_trow_src = reinterpret_cast<const uint16_t**>(base + o_offl_t);
+    p.d_offload_tmaps = reinterpret_cast<unsigned char*>(base + o_offl_t);
     if ((e = put(o_offl_s, tbl.data(), n_slots * sizeof(void*))) != cudaSuccess ||
-        (e = put(o_offl_t, trs.data(), n_trows * sizeof(void*))) != cudaSuccess)
+        (e = put(o_offl_t, maps.data(), n_slots * kTmapBytes)) != cudaSuccess)
       return cuda_fail(e, "uploading offload tables");
+    p.offload_tmaps_dirty = true;
   }
   return WT_OK;
 }
 
 // Check the caller's pointers and, when they changed since the last call,
-// rebuild the dynamic pointer block (shard pointers, block-row sources,
-// absolute destination addresses) on the host and queue one copy on s.
+// rebuild the dynamic pointer block (shard pointers, the shards' tensor
+// maps, absolute destination addresses) on the host and queue one copy on s.
 wt_status stage_pointers(Plan& p, const void* const* shards, void* const* pools, cudaStream_t s) {
   const size_t n_slots = (size_t)p.num_slots, n_ranks = (size_t)p.num_ranks;
   const bool shards_changed =
@@ -198,7 +200,12 @@ wt_status stage_pointers(Plan& p, const void* const* shards, void* const* pools,
   char* h = static_cast<char*>(p.h_pinned);
   if (shards_changed) {
     std::memcpy(h + dl.shards, shards, n_slots * sizeof(void*));
-    fill_trow_src(p, shards, reinterpret_cast<const uint16_t**>(h + dl.trows));
+    wt_status st = encode_tmaps(p, shards, reinterpret_cast<unsigned char*>(h + dl.tmaps));
+    if (st != WT_OK) {
+      p.shards_valid = false;
+      return st;
+    }
+    p.tmaps_dirty = true;
   }
   if (pools_changed) {
     DevDstPtr* dp = reinterpret_cast<DevDstPtr*>(h + dl.dsts);
@@ -225,9 +232,9 @@ wt_status stage_pointers(Plan& p, const void* const* shards, void* const* pools,
   return WT_OK;
 }
 
+// One persistent CTA per SM (each holds a 128 KiB shared-memory ring).
 int grid_for(const Plan& p, int64_t units) {
-  const int64_t full = (int64_t)p.sm_count * p.grid_per_sm;
-  return (int)std::max<int64_t>(1, std::min<int64_t>(units, full));
+  return (int)std::max<int64_t>(1, std::min<int64_t>(units, p.sm_count));
 }
 
 }  // namespace
@@ -316,11 +323,13 @@ wt_status wt_prepare(wt_plan* h, const void* const* shard_ptrs, void* const* poo
   if (st != WT_OK) return st;
   PrepArgs a = p.args;
   a.shard_ptrs = p.d_shard_ptrs;
-  a.trow_src = p.d_trow_src;
+  a.tmaps = p.d_tmaps;
+  a.tmap_fence = p.tmaps_dirty ? 1u : 0u;
   a.unit_begin = 0;
   a.unit_end = p.num_units;
   cudaError_t e = launch_prepare(a, grid_for(p, p.num_units), s, p.flags & WT_FLAG_DEBUG_CHECKS);
   if (e != cudaSuccess) return cuda_fail(e, "preparation kernel launch");
+  p.tmaps_dirty = false;
   if ((e = cudaEventRecord(p.last_done, s)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
   p.ran = true;
   return WT_OK;
@@ -342,7 +351,7 @@ wt_status wt_prepare_offload(wt_plan* h, const void* host_image, void* const* po
   if (st != WT_OK) return st;
   PrepArgs a = p.args;
   a.shard_ptrs = p.d_offload_shard_ptrs;
-  a.trow_src = p.d_offload_trow_src;
+  a.tmaps = p.d_offload_tmaps;
   const char* host = static_cast<const char*>(host_image);
   auto drain = [&](wt_status s_, const std::string& msg) {
     cudaStreamSynchronize(cs);
@@ -367,9 +376,11 @@ wt_status wt_prepare_offload(wt_plan* h, const void* host_image, void* const* po
       return drain(WT_ERR_CUDA, std::string("event: ") + cudaGetErrorString(e));
     a.unit_begin = c.unit_begin;
     a.unit_end = c.unit_end;
+    a.tmap_fence = p.offload_tmaps_dirty ? 1u : 0u;
     if ((e = launch_prepare(a, grid_for(p, c.unit_end - c.unit_begin), ks,
                             p.flags & WT_FLAG_DEBUG_CHECKS)) != cudaSuccess)
       return drain(WT_ERR_CUDA, std::string("preparation kernel launch: ") + cudaGetErrorString(e));
+    if (c.unit_end > c.unit_begin) p.offload_tmaps_dirty = false;
     if ((e = cudaEventRecord(p.prep_done[b], ks)) != cudaSuccess)
       return drain(WT_ERR_CUDA, std::string("cudaEventRecord: ") + cudaGetErrorString(e));
     p.prep_recorded[b] = true;
@@ -391,6 +402,8 @@ wt_status wt_plan_check(wt_plan* h, void* stream) {
     return cuda_fail(e, "reading the error word");
   if (word) {
     cudaMemset(p.d_error, 0, sizeof(int32_t));
+    if (word & kErrTimeout)
+      return fail(WT_ERR_TIMEOUT, "a wait inside the preparation kernel gave up; its output is incomplete");
     return fail(WT_ERR_INTERNAL, "a store fell outside its destination range");
   }
   return WT_OK;

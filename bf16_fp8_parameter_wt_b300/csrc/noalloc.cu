@@ -30,7 +30,6 @@ constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 void* g_scratch_addr[kMaxDevices] = {};   // device address of the array, per device
 int g_sm_count[kMaxDevices] = {};
-int g_blocks_per_sm[kMaxDevices] = {};
 
 size_t up256(size_t v) { return (v + 255) & ~size_t(255); }
 
@@ -52,8 +51,9 @@ wt_status device_setup(int device) {
   int sms = 0;
   e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
   if (e != cudaSuccess) return fail_na(WT_ERR_CUDA, std::string("cudaDeviceGetAttribute: ") + cudaGetErrorString(e));
+  if ((e = prep_kernel_setup()) != cudaSuccess)
+    return fail_na(WT_ERR_CUDA, std::string("preparation kernel set-up: ") + cudaGetErrorString(e));
   g_sm_count[device] = sms;
-  g_blocks_per_sm[device] = prep_blocks_per_sm();
   g_scratch_addr[device] = ptr;
   return WT_OK;
 }
@@ -74,16 +74,15 @@ extern "C" wt_status wt_prepare_noalloc(const wt_plan_desc* desc, const void* co
   wt_status st = compile_plan(desc, &p);
   if (st != WT_OK) return st;
 
-  // table image: shard pointers, block-row sources, destinations, unit
-  // descriptors, runs, first run per block row, error word
-  const size_t n_slots = (size_t)p.num_slots, n_trows = p.h_trows.size();
+  // table image: shard pointers, their tensor maps, destinations, unit
+  // descriptors, row runs, error word
+  const size_t n_slots = (size_t)p.num_slots;
   const size_t o_shards = 0;
-  const size_t o_trows = up256(o_shards + n_slots * sizeof(void*));
-  const size_t o_dsts = up256(o_trows + n_trows * sizeof(void*));
+  const size_t o_tmaps = up256(o_shards + n_slots * sizeof(void*));
+  const size_t o_dsts = up256(o_tmaps + n_slots * kTmapBytes);
   const size_t o_units = up256(o_dsts + (size_t)p.num_dst_entries * sizeof(DevDstPtr));
   const size_t o_runs = up256(o_units + p.h_units.size() * sizeof(DevUnit));
-  const size_t o_tfr = up256(o_runs + p.h_runs.size() * sizeof(DevRun));
-  const size_t o_err = up256(o_tfr + n_trows * sizeof(int32_t));
+  const size_t o_err = up256(o_runs + p.h_runs.size() * sizeof(DevRun));
   const size_t total = o_err + 256;
   if (total > kNoAllocScratchBytes)
     return fail_na(WT_ERR_INVALID_ARGUMENT,
@@ -118,8 +117,10 @@ extern "C" wt_status wt_prepare_noalloc(const wt_plan_desc* desc, const void* co
 
   std::vector<unsigned char> img(total, 0);   // host image; the error word starts at zero
   unsigned char* h = img.data();
-  if (n_slots) std::memcpy(h + o_shards, shard_ptrs, n_slots * sizeof(void*));
-  fill_trow_src(p, shard_ptrs, reinterpret_cast<const uint16_t**>(h + o_trows));
+  if (n_slots) {
+    std::memcpy(h + o_shards, shard_ptrs, n_slots * sizeof(void*));
+    if ((st = encode_tmaps(p, shard_ptrs, h + o_tmaps)) != WT_OK) return st;
+  }
   DevDstPtr* dp = reinterpret_cast<DevDstPtr*>(h + o_dsts);
   for (const OutputInfo& oi : p.outputs)
     for (size_t k = 0; k < oi.dsts.size(); ++k) {
@@ -133,8 +134,6 @@ extern "C" wt_status wt_prepare_noalloc(const wt_plan_desc* desc, const void* co
     }
   if (!p.h_units.empty()) std::memcpy(h + o_units, p.h_units.data(), p.h_units.size() * sizeof(DevUnit));
   if (!p.h_runs.empty()) std::memcpy(h + o_runs, p.h_runs.data(), p.h_runs.size() * sizeof(DevRun));
-  if (!p.h_trow_first_run.empty())
-    std::memcpy(h + o_tfr, p.h_trow_first_run.data(), p.h_trow_first_run.size() * sizeof(int32_t));
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   // from pageable memory: the call returns once the image has been staged
@@ -143,16 +142,16 @@ extern "C" wt_status wt_prepare_noalloc(const wt_plan_desc* desc, const void* co
 
   PrepArgs a{};
   a.units = reinterpret_cast<const DevUnit*>(dbase + o_units);
-  a.trow_src = reinterpret_cast<const uint16_t* const*>(dbase + o_trows);
-  a.trow_first_run = reinterpret_cast<const int32_t*>(dbase + o_tfr);
+  a.tmaps = reinterpret_cast<const unsigned char*>(dbase + o_tmaps);
+  a.tmap_fence = 1;                    // the maps were just rewritten
+  a.timeout_ns = kDefaultTimeoutNs;
   a.runs = reinterpret_cast<const DevRun*>(dbase + o_runs);
   a.shard_ptrs = reinterpret_cast<const uint16_t* const*>(dbase + o_shards);
   a.dst_ptrs = reinterpret_cast<const DevDstPtr*>(dbase + o_dsts);
   a.unit_begin = 0;
   a.unit_end = p.num_units;
   a.error_word = reinterpret_cast<int32_t*>(dbase + o_err);
-  const int64_t full = (int64_t)g_sm_count[device] * g_blocks_per_sm[device];
-  const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(p.num_units, full));
+  const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(p.num_units, g_sm_count[device]));
   e = launch_prepare(a, grid, s, false);
   if (e != cudaSuccess) return fail_na(WT_ERR_CUDA, std::string("preparation kernel launch: ") + cudaGetErrorString(e));
   return WT_OK;

@@ -205,12 +205,19 @@ wt_status compile_plan(const wt_plan_desc* d, Plan* p) {
                                              std::to_string(p->pool_bytes[r]) + " bytes");
   }
 
-  // ---- device tables: units, row runs, block rows ------------------------
+  // ---- device tables: units, row runs, per-slot shapes -------------------
   p->h_units.clear();
   p->h_runs.clear();
-  p->h_trows.clear();
-  p->h_trow_first_run.clear();
   p->h_units.reserve((size_t)units);
+  p->slot_rows.assign(p->num_slots, 0);
+  p->slot_cols.assign(p->num_slots, 0);
+  p->slot_tmap.assign(p->num_slots, 0);
+  for (const auto& pi : p->params)
+    for (size_t s = 0; s < pi.shard_rows.size(); ++s) {
+      p->slot_rows[pi.slot_base + s] = pi.shard_rows[s];
+      p->slot_cols[pi.slot_base + s] = pi.cols;
+      p->slot_tmap[pi.slot_base + s] = p->outputs[pi.output].vec && pi.shard_rows[s] > 0;
+    }
   int32_t dst_entries = 0;
   for (int o = 0; o < (int)p->outputs.size(); ++o) {
     auto& oi = p->outputs[o];
@@ -237,20 +244,16 @@ wt_status compile_plan(const wt_plan_desc* d, Plan* p) {
       const int64_t r0 = bi * kTile;
       const int64_t nrows = std::min<int64_t>(kTile, oi.rows - r0);
       while (p->h_runs[k].row0 + p->h_runs[k].rows <= r0) ++k;
-      TileRowInfo tr;
-      tr.output = o;
-      tr.first_run = (int32_t)k;
-      tr.single = p->h_runs[k].row0 + p->h_runs[k].rows >= r0 + nrows;
-      tr.row_in_run = r0 - p->h_runs[k].row0;
-      const uint32_t gtr = (uint32_t)p->h_trows.size();
-      p->h_trows.push_back(tr);
-      p->h_trow_first_run.push_back((int32_t)k);
-      const uint32_t f = flags | (tr.single ? 0u : kUnitMulti);
+      const DevRun& run = p->h_runs[k];
+      const bool single = run.row0 + run.rows >= r0 + nrows;
+      // one shard and 16-byte rows: one 2-D tensor copy from that shard
+      const bool tma = single && oi.vec;
+      const uint32_t f = flags | (single ? 0u : kUnitMulti);
       for (int64_t bj = 0; bj < tiles_n; ++bj) {
         const int64_t ncols = std::min<int64_t>(kTile, oi.cols - bj * kTile);
         DevUnit u;
-        u.o = (uint32_t)o;
-        u.gtr = gtr;
+        u.src = tma ? (uint32_t)run.slot : (uint32_t)k;
+        u.src_row = tma ? (uint32_t)(r0 - run.row0) : (uint32_t)r0;
         u.bi = (uint32_t)bi;
         u.bj = (uint32_t)bj;
         u.cols = (uint32_t)oi.cols;
@@ -304,19 +307,6 @@ wt_status compile_plan(const wt_plan_desc* d, Plan* p) {
     }
   }
   return WT_OK;
-}
-
-void fill_trow_src(const Plan& p, const void* const* shards, const uint16_t** out) {
-  for (size_t g = 0; g < p.h_trows.size(); ++g) {
-    const TileRowInfo& tr = p.h_trows[g];
-    if (!tr.single) {
-      out[g] = nullptr;
-      continue;
-    }
-    const DevRun& run = p.h_runs[tr.first_run];
-    const uint16_t* base = static_cast<const uint16_t*>(shards[run.slot]);
-    out[g] = base + tr.row_in_run * p.outputs[tr.output].cols;
-  }
 }
 
 }  // namespace wt

@@ -15,18 +15,27 @@
 namespace wt {
 
 constexpr int kTile = 128;        // block edge (rows and cols)
-constexpr int kThreads = 256;     // threads per CTA of the preparation kernel
+constexpr int kTmapBytes = 128;   // one CUtensorMap
 
 // DevUnit.shape flag bits (bits 16..23)
 constexpr uint32_t kUnitFp8 = 1u;    // e4m3 codes + scale, else BF16 bytes
-constexpr uint32_t kUnitVec = 2u;    // 16-byte vector path, else element path
+constexpr uint32_t kUnitVec = 2u;    // rows are 16-byte aligned: bulk-copy path, else element path
 constexpr uint32_t kUnitMulti = 4u;  // block rows come from more than one shard
 
+// Error word bits set by the kernel
+constexpr int32_t kErrBadStore = 1;  // debug checks: a store fell outside its pool range
+constexpr int32_t kErrTimeout = 2;   // a bounded wait gave up
+
 // Static descriptor of one 128x128 work unit, 32 bytes (eight words that
-// one warp fetches with one coalesced load).
+// one warp fetches with one coalesced load). Where the block's rows come
+// from:
+//   vec, one shard  : src = shard slot (its tensor map), src_row = first
+//                     row of the block inside that shard;
+//   otherwise       : src = first row run that touches the block, src_row =
+//                     first fused row of the block (bi * 128).
 struct DevUnit {
-  uint32_t o;          // output index
-  uint32_t gtr;        // global block-row index (source pointer tables)
+  uint32_t src;
+  uint32_t src_row;
   uint32_t bi, bj;     // block row / column inside the output
   uint32_t cols;       // N: elements per row of the output
   uint32_t shape;      // (nrows - 1) | (ncols - 1) << 8 | flags << 16
@@ -57,13 +66,14 @@ static_assert(sizeof(DevDstPtr) == 32, "layout");
 // Everything one launch of the preparation kernel reads.
 struct PrepArgs {
   const DevUnit* units;
-  const uint16_t* const* trow_src;   // per block row: address of its first row (one-shard rows)
-  const int32_t* trow_first_run;     // per block row: first run touching it (multi-shard rows)
   const DevRun* runs;
   const uint16_t* const* shard_ptrs;
+  const unsigned char* tmaps;        // kTmapBytes per slot, 64-byte aligned
   const DevDstPtr* dst_ptrs;
   int64_t unit_begin, unit_end;
-  int32_t* error_word;               // debug checks: set to 1 on a bad store
+  int32_t* error_word;               // kErr* bits
+  uint64_t timeout_ns;               // limit of every wait inside the kernel
+  uint32_t tmap_fence;               // tensor maps were rewritten since the last launch
 };
 
 // Host-side copy of one param.
@@ -92,14 +102,6 @@ struct OutputInfo {
   bool vec = false;
 };
 
-// Host view of one block row, used to rebuild its source address.
-struct TileRowInfo {
-  int32_t output = 0;
-  int32_t first_run = 0;    // index into runs
-  bool single = true;       // all of its rows come from runs[first_run]
-  int64_t row_in_run = 0;   // first row of the block row, relative to the run
-};
-
 // An offload chunk: a run of whole outputs, contiguous in the host image.
 struct Chunk {
   int32_t out_begin = 0, out_end = 0;
@@ -126,15 +128,17 @@ struct Plan {
   // host images of the static device tables
   std::vector<DevUnit> h_units;
   std::vector<DevRun> h_runs;
-  std::vector<TileRowInfo> h_trows;
-  std::vector<int32_t> h_trow_first_run;
+  // per slot: rows and cols of the shard, and whether a tensor map is
+  // encoded for it (vec outputs, non-empty shards)
+  std::vector<int64_t> slot_rows, slot_cols;
+  std::vector<uint8_t> slot_tmap;
 
   // device side: one allocation for the static tables, one for the
   // pointer tables that follow the caller's buffers
   void* d_tables = nullptr;
   PrepArgs args{};                   // static parts filled at upload
   const uint16_t** d_shard_ptrs = nullptr;      // dynamic block: shard ptrs,
-  const uint16_t** d_trow_src = nullptr;        //   block-row sources,
+  unsigned char* d_tmaps = nullptr;             //   their tensor maps,
   DevDstPtr* d_dst_ptrs = nullptr;              //   destination pointers
   size_t dyn_bytes = 0;                         // size of that block
   int32_t* d_error = nullptr;
@@ -142,11 +146,11 @@ struct Plan {
   std::vector<const void*> cached_shards;
   std::vector<void*> cached_pools;
   bool shards_valid = false, pools_valid = false;
+  bool tmaps_dirty = false;          // rewritten since the last launch
   cudaEvent_t ptr_upload_done = nullptr;
   cudaEvent_t last_done = nullptr;
   bool ran = false;
   int sm_count = 0;
-  int grid_per_sm = 3;
 
   // offload
   uint64_t chunk_bytes = 0;
@@ -154,7 +158,8 @@ struct Plan {
   uint64_t staging_bytes = 0;
   void* staging[2] = {nullptr, nullptr};
   const uint16_t** d_offload_shard_ptrs = nullptr;
-  const uint16_t** d_offload_trow_src = nullptr;
+  unsigned char* d_offload_tmaps = nullptr;
+  bool offload_tmaps_dirty = false;
   cudaEvent_t h2d_done[2] = {nullptr, nullptr};
   cudaEvent_t prep_done[2] = {nullptr, nullptr};
   bool prep_recorded[2] = {false, false};
@@ -163,13 +168,20 @@ struct Plan {
 
 // plan.cpp
 wt_status compile_plan(const wt_plan_desc* d, Plan* p);   // host only
-// Source address of every block row, given the shard address of every slot.
-void fill_trow_src(const Plan& p, const void* const* shards, const uint16_t** out);
 void set_error(const std::string& msg);
 
+// tmap.cpp: the 2-D tensor map of every slot that has one (zeros for the
+// others), kTmapBytes each, into out (64-byte aligned).
+wt_status encode_tmaps(const Plan& p, const void* const* shards, unsigned char* out);
+
 // prep_kernel.cu
+constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;   // 2 s per wait
+// One-time per-device set-up of the kernel (shared-memory size); call with
+// the device current.
+cudaError_t prep_kernel_setup();
+// Launch over units [a.unit_begin, a.unit_end) with grid CTAs (at most one
+// per SM is resident).
 cudaError_t launch_prepare(const PrepArgs& a, int grid, cudaStream_t s, bool debug);
-int prep_blocks_per_sm();
 
 }  // namespace wt
 

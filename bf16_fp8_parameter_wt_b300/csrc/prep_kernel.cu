@@ -10,32 +10,51 @@
 // shards). FP8 = e4m3 "fn", RNE, saturating; scale = amax / 448 as an IEEE
 // binary32 division, 1.0 for an all-zero block; code = e4m3(fl32(x / scale)).
 //
-// Mapping. A CTA of 256 threads owns one unit at a time (persistent grid,
-// units strided by gridDim.x). Thread t owns the 16-byte column chunk
-// t % 16 of the rows t / 16 + 16 i, i = 0..7, so a warp reads two full
-// 256-byte block rows per load instruction and the block stays in
-// registers between the amax and the quantisation (one HBM read per byte).
+// Structure (one persistent CTA per SM, units strided by the grid):
+//   - a producer warp moves each unit's BF16 block into a ring of four
+//     32 KiB shared-memory stages with the tensor memory accelerator: one
+//     2-D tensor copy when all 128 rows come from one shard, one 1-D bulk
+//     copy per row when they come from several (the full_tensor() row
+//     gather), nothing when rows are not 16-byte aligned (the consumers
+//     then gather those elements themselves). Full/empty mbarriers order
+//     the ring; the producer runs up to four units ahead, so HBM reads
+//     stay in flight while the consumers compute.
+//   - two consumer groups of four warps take alternate units. Thread t of a
+//     group owns the 16-byte column chunk t % 16 of the rows t / 16 + 8 j,
+//     j = 0..15 (with G threads per group: rows t / 16 + (G / 16) j): it
+//     loads them from shared memory (conflict-free, two full
+//     256-byte rows per warp instruction), reduces |x| with packed bf16x2
+//     abs-max, a warp shuffle and one named barrier, quantises from
+//     registers, releases the stage and stores full 128-byte code lines.
+//     Each HBM byte is read once. That straight-line path covers a whole
+//     block of 16-byte rows with one destination (every block of the big
+//     workloads); partial blocks, unaligned rows, several destinations,
+//     extreme scales and debug checks go through general routines that
+//     re-read the thread's rows from the stage before releasing it, so
+//     their code stays out of the hot path's registers.
 //
-// Pipelining. Warp 0 fetches the 32-byte descriptor of the unit two steps
-// ahead and the source / destination addresses of the unit one step ahead,
-// and publishes them in a shared-memory ring before the per-unit barrier,
-// so no thread waits on a dependent metadata load. The data loads of the
-// next unit are issued as soon as the current unit's codes are computed,
-// so they are in flight while the current unit is being stored.
+// Division. The code of x must be E(fl32(x / s)). The scale is the same for
+// the whole block, so the kernel forms r = RN(1/s) once and gets each
+// quotient with one reciprocal-based correction step (Markstein):
+//   q0 = RN(x r),  e = x - q0 s (one fma),  y = fma(e, r, q0).
+// q0 is within one ulp of x/s, so the remainder e = x - q0 s is exact, and
+// y = RN(x/s + (x/s - q0) d) where d, the relative error of r, is at most
+// 2^-24: y differs from fl32(x/s) only if x/s lies within 2^-47 (relative)
+// of a binary32 rounding boundary without being on it. x/s can never sit
+// exactly on such a boundary (x has 8 significant bits, s 24), and exact
+// e4m3 ties (x/s equal to an e4m3 midpoint, which BF16 inputs hit often)
+// are binary32 numbers, which the correction reproduces exactly. Whether a
+// near-boundary quotient exists is settled by the GPU test that runs every
+// pair (block amax, element) of BF16 values through this path and compares
+// each code with the CPU oracle's division. The remainder is exact only
+// while it stays normal, so blocks with s < 2^-87 (amax < 4.5e-24) or a
+// subnormal 1/s take the IEEE division instead; below that range x/s
+// rounds to a signed zero code on both paths.
 //
-// Division. The code of x must be E(fl32(x / s)). Dividing every element
-// is an ALU-heavy sequence, so the kernel brackets the quotient instead:
-// with r = RN(1/s), rlo = RN(r (1 - 2^-21)) and rhi = RN(r (1 + 2^-21)),
-// ylo = RN(x rlo) and yhi = RN(x rhi) satisfy |ylo| < |fl32(x/s)| < |yhi|
-// whenever the values are normal (each RN adds a relative error of at
-// most 2^-24, five of them stay below the 2^-21 margin), and all three
-// share the sign of x. E is monotone in |y|, so when E(ylo) == E(yhi) that
-// code is E(fl32(x/s)). Otherwise (a rounding boundary of E lies inside
-// the bracket, about once per 2^17 elements, or exactly on a tie) the
-// chunk is recomputed with the IEEE division. Subnormal results are far
-// below the smallest e4m3 step and encode to a signed zero on every path.
-// Blocks whose scale or reciprocal would be subnormal use the IEEE
-// division throughout.
+// Waits. Every mbarrier wait gives up after PrepArgs::timeout_ns; the role
+// that gives up sets kErrTimeout in the error word and an abort flag in
+// shared memory, the others notice it and leave, and the producer first
+// waits (bounded) for its copies in flight to land.
 #include <cuda_fp8.h>
 
 #include "plan.h"
@@ -43,38 +62,138 @@
 namespace wt {
 namespace {
 
-constexpr int kWarps = kThreads / 32;
-constexpr int kRowsPerThread = kTile * kTile / 8 / kThreads;   // 8
-constexpr int kMetaSlots = 4;
+constexpr int kGroups = 2;                          // consumer groups
+constexpr int kGroupWarps = 4;
+constexpr int kGroupThreads = 32 * kGroupWarps;
+constexpr int kStages = 4;                          // ring depth
+// Unit k uses stage k % kStages and group k % kGroups. Each stage must
+// belong to one group: a parity wait on an mbarrier is only meaningful
+// when the waiter has already seen the previous phase complete, which a
+// group guarantees for its own stages by taking their units in order.
+static_assert(kStages % kGroups == 0, "every stage must belong to one consumer group");
+constexpr int kStageBytes = kTile * kTile * 2;      // one BF16 block
+constexpr int kRowBytes = kTile * 2;                // one block row in a stage
+constexpr int kConsumerThreads = kGroups * kGroupThreads;
+constexpr int kCtaThreads = kConsumerThreads + 32;
+constexpr int kRowStride = kGroupThreads / 16;      // rows between a thread's rows
+constexpr int kRows = kTile / kRowStride;           // rows per consumer thread
 constexpr unsigned kFull = 0xFFFFFFFFu;
+// biased exponents of the scales the correction step handles: 2^-87 <= s
+// and 1/s normal
+constexpr uint32_t kMinScaleExp = 40u, kMaxScaleExp = 252u;
 
-// Shared-memory metadata slot (16 words):
-//   0..7   the unit's DevUnit
-//   8, 9   source address of its block row (one-shard rows)
-//   10..13 data and scale addresses of its first destination
-constexpr int kMetaWords = 16;
+struct SmemCtl {
+  DevUnit meta[kStages];                 // the unit in each stage
+  uint64_t full[kStages];                // producer -> consumers
+  uint64_t empty[kStages];               // consumers -> producer
+  float wmax[kGroups][2][kGroupWarps];   // per-warp block amax, double-buffered
+  int abort_flag;
+};
+constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kStageBytes + sizeof(SmemCtl);
+static_assert(kSmemBytes <= 227 * 1024, "shared memory");
 
-__device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
-  uint4 v;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p));
-  return v;
+// ---------------------------------------------------------------- PTX ---
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
 }
 
-__device__ __forceinline__ uint16_t ld_stream_u16(const uint16_t* p) {
-  uint16_t v;
-  asm volatile("ld.global.nc.L1::no_allocate.u16 %0, [%1];" : "=h"(v) : "l"(p));
-  return v;
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
 }
 
-__device__ __forceinline__ uint32_t ld_meta_u32(const void* p) {
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ uint64_t globaltimer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ uint64_t evict_first_policy() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+// One 128x128 BF16 box of a 2-D tensor map into a stage.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* map, int x, int y, uint32_t bar,
+                                            uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+      "l"(map), "r"(x), "r"(y), "r"(bar), "l"(pol)
+      : "memory");
+}
+
+// A contiguous run of bytes (multiple of 16, both ends 16-byte aligned).
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar,
+                                          uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1], %2, [%3], %4;" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(bar), "l"(pol)
+      : "memory");
+}
+
+// The host rewrote this tensor map since the last launch.
+__device__ __forceinline__ void tmap_acquire(const void* map) {
+  asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"(map) : "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void bar_sync(int id, int n) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
+// Named barrier that also ORs a flag over its threads.
+__device__ __forceinline__ bool bar_red_or(int id, int n, bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 q, %1, 0;\n\t"
+      "bar.red.or.pred p, %2, %3, q;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)v), "r"(id), "r"(n)
+      : "memory");
+  return r != 0;
+}
+
+__device__ __forceinline__ uint32_t ld_nc_u32(const void* p) {
   uint32_t v;
   asm volatile("ld.global.nc.u32 %0, [%1];" : "=r"(v) : "l"(p));
   return v;
 }
 
-// max(|a|, |b|) per bf16 half; the sign bits of the result are meaningless
+__device__ __forceinline__ uint16_t ld_nc_u16(const void* p) {
+  uint16_t v;
+  asm volatile("ld.global.nc.L1::no_allocate.u16 %0, [%1];" : "=h"(v) : "l"(p));
+  return v;
+}
+
+// max(|a|, |b|) per bf16 half; the result's sign bits are meaningless
 // (xorsign), only magnitudes are kept.
 __device__ __forceinline__ uint32_t absmax_bf16x2(uint32_t a, uint32_t b) {
   uint32_t d;
@@ -90,327 +209,396 @@ __device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
   return (uint32_t)__nv_cvt_float2_to_fp8x2(make_float2(lo, hi), __NV_SATFINITE, __NV_E4M3);
 }
 
-// 8 BF16 elements (one 16-byte chunk) -> 8 codes with the IEEE division.
-__device__ __noinline__ uint2 quant_chunk_exact(uint4 v, float s) {
-  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-  uint32_t c[4];
-#pragma unroll
-  for (int k = 0; k < 4; ++k)
-    c[k] = e4m3x2(__fdiv_rn(bf16_lo(w[k]), s), __fdiv_rn(bf16_hi(w[k]), s));
-  return make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
-}
-
-// The bracketed version; returns false if any of the 8 codes is uncertain.
-__device__ __forceinline__ bool quant_chunk_bracket(const uint4& v, float rlo, float rhi, uint2& out) {
-  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-  uint32_t c[4], diff = 0;
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const float x0 = bf16_lo(w[k]), x1 = bf16_hi(w[k]);
-    const uint32_t clo = e4m3x2(x0 * rlo, x1 * rlo);
-    const uint32_t chi = e4m3x2(x0 * rhi, x1 * rhi);
-    diff |= clo ^ chi;
-    c[k] = clo;
+// --------------------------------------------------------- waits, abort ---
+// Wait for the phase of parity `parity`; false when it has not completed
+// within limit_ns, or (abort_flag given) another role gave up.
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, uint64_t limit_ns,
+                                             const volatile int* abort_flag) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 15u) == 0) {
+      if (abort_flag && *abort_flag) return false;
+      if (globaltimer() - t0 > limit_ns) return false;
+    }
   }
-  out = make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
-  return diff == 0;
 }
 
-// Per-thread view of one unit's metadata (read from the shared ring).
-struct Meta {
-  uint32_t bi, bj, N, shape, num_dsts, dst_begin, gtr;
-  const uint16_t* src;
-  uint8_t* dst0;
-  float* scale0;
-  __device__ __forceinline__ int nrows() const { return (int)(shape & 0xFFu) + 1; }
-  __device__ __forceinline__ int ncols() const { return (int)((shape >> 8) & 0xFFu) + 1; }
-  __device__ __forceinline__ uint32_t flags() const { return shape >> 16; }
-};
-
-__device__ __forceinline__ Meta read_meta(const uint32_t* s) {
-  const uint4 a = *reinterpret_cast<const uint4*>(s);
-  const uint4 b = *reinterpret_cast<const uint4*>(s + 4);
-  const uint4 c = *reinterpret_cast<const uint4*>(s + 8);
-  const uint4 d = *reinterpret_cast<const uint4*>(s + 12);
-  Meta m;
-  m.gtr = a.y;
-  m.bi = a.z;
-  m.bj = a.w;
-  m.N = b.x;
-  m.shape = b.y;
-  m.num_dsts = b.z;
-  m.dst_begin = b.w;
-  m.src = reinterpret_cast<const uint16_t*>(((uint64_t)c.y << 32) | c.x);
-  m.dst0 = reinterpret_cast<uint8_t*>(((uint64_t)c.w << 32) | c.z);
-  m.scale0 = reinterpret_cast<float*>(((uint64_t)d.y << 32) | d.x);
-  return m;
+__device__ __forceinline__ void give_up(const PrepArgs& a, SmemCtl& sm) {
+  *reinterpret_cast<volatile int*>(&sm.abort_flag) = 1;
+  atomicOr(a.error_word, kErrTimeout);
 }
 
-// Warp 0, lanes 0..7: word `lane` of the descriptor of unit u (0 past the end).
-__device__ __forceinline__ uint32_t fetch_unit_word(const PrepArgs& a, int64_t u, int lane) {
-  if (lane >= 8 || u >= a.unit_end) return 0;
-  return ld_meta_u32(reinterpret_cast<const uint32_t*>(a.units + u) + lane);
+// --------------------------------------------------------------- producer ---
+__device__ __forceinline__ uint32_t load_unit_word(const PrepArgs& a, int64_t first, int64_t n_local,
+                                                   int64_t batch, int lane) {
+  const int64_t k = 4 * batch + (lane >> 3);
+  if (k >= n_local) return 0;
+  const int64_t u = first + k * (int64_t)gridDim.x;
+  return ld_nc_u32(reinterpret_cast<const uint32_t*>(a.units + u) + (lane & 7));
 }
 
-// Warp 0, lanes 8..13: the dynamic words of the unit whose descriptor words
-// lanes 0..7 hold in w.
-__device__ __forceinline__ uint32_t fetch_dyn_word(const PrepArgs& a, uint32_t w, int lane, bool valid) {
-  const uint32_t gtr = __shfl_sync(kFull, w, 1);
-  const uint32_t dst_begin = __shfl_sync(kFull, w, 7);
-  if (!valid) return 0;
-  if (lane == 8 || lane == 9)
-    return ld_meta_u32(reinterpret_cast<const uint32_t*>(a.trow_src + gtr) + (lane - 8));
-  if (lane >= 10 && lane < 14)
-    return ld_meta_u32(reinterpret_cast<const uint32_t*>(a.dst_ptrs + dst_begin) + (lane - 10));
-  return 0;
+__device__ void producer(const PrepArgs& a, SmemCtl& sm, uint32_t stage0, int64_t first, int64_t n_local,
+                         int lane) {
+  const uint64_t pol = evict_first_policy();
+  // descriptors of four consecutive units per batch: lane l holds word
+  // l % 8 of unit l / 8; two batches are always in flight ahead
+  uint32_t cur = load_unit_word(a, first, n_local, 0, lane);
+  uint32_t nxt = load_unit_word(a, first, n_local, 1, lane);
+  int64_t last_slot = -1;
+  int64_t k = 0;
+  bool ok = true;
+  for (int64_t b = 0; ok && k < n_local; ++b) {
+    const uint32_t nn = load_unit_word(a, first, n_local, b + 2, lane);
+    for (int j = 0; j < 4 && k < n_local; ++j, ++k) {
+      uint32_t w[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) w[i] = __shfl_sync(kFull, cur, 8 * j + i);
+      const int st = (int)(k % kStages);
+      const uint32_t full = smem_u32(&sm.full[st]);
+      bool got = true;
+      if (lane == 0) got = wait_bounded(smem_u32(&sm.empty[st]), (uint32_t)((k / kStages) & 1) ^ 1u,
+                                        a.timeout_ns, &sm.abort_flag);
+      if (!__shfl_sync(kFull, (int)got, 0)) {
+        if (lane == 0) give_up(a, sm);
+        ok = false;
+        break;
+      }
+      const uint32_t flags = w[5] >> 16;
+      const uint32_t dst = stage0 + (uint32_t)st * kStageBytes;
+      if (lane == 0) {
+        uint4* m = reinterpret_cast<uint4*>(&sm.meta[st]);
+        m[0] = make_uint4(w[0], w[1], w[2], w[3]);
+        m[1] = make_uint4(w[4], w[5], w[6], w[7]);
+      }
+      if (!(flags & kUnitVec)) {
+        if (lane == 0) mbar_arrive(full);          // the consumers gather this one
+      } else if (!(flags & kUnitMulti)) {
+        if (lane == 0) {
+          const unsigned char* map = a.tmaps + (size_t)w[0] * kTmapBytes;
+          if (a.tmap_fence && (int64_t)w[0] != last_slot) tmap_acquire(map);
+          last_slot = w[0];
+          mbar_arrive_tx(full, kStageBytes);
+          tma_load_2d(dst, map, (int)(w[3] * kTile), (int)w[1], full, pol);
+        }
+      } else {
+        // rows from several shards: one bulk copy per row
+        const int nrows = (int)(w[5] & 0xFFu) + 1;
+        const uint32_t row_bytes = (((w[5] >> 8) & 0xFFu) + 1u) * 2u;
+        if (lane == 0) mbar_arrive_tx(full, row_bytes * (uint32_t)nrows);
+        __syncwarp();
+        const int64_t N = w[4];
+        int run = (int)w[0];
+        for (int r = lane; r < nrows; r += 32) {
+          const int64_t fr = (int64_t)w[1] + r;
+          while (fr >= a.runs[run].row0 + a.runs[run].rows) ++run;
+          const DevRun rn = a.runs[run];
+          const uint16_t* src = a.shard_ptrs[rn.slot] + (fr - rn.row0) * N + (int64_t)w[3] * kTile;
+          bulk_load(dst + (uint32_t)r * kRowBytes, src, row_bytes, full, pol);
+        }
+      }
+    }
+    cur = nxt;
+    nxt = nn;
+  }
+  // no copy may still be landing in this CTA's shared memory when it exits:
+  // wait for the last fill of every stage (completed fills return at once)
+  if (lane == 0) {
+    for (int st = 0; st < kStages && st < k; ++st) {
+      const int64_t last = st + ((k - 1 - st) / kStages) * kStages;
+      if (!wait_bounded(smem_u32(&sm.full[st]), (uint32_t)((last / kStages) & 1), a.timeout_ns, nullptr))
+        give_up(a, sm);
+    }
+  }
+  __syncwarp();
 }
 
+// -------------------------------------------------------------- consumers ---
 template <bool kDebug>
-__device__ __forceinline__ bool store_ok(const PrepArgs& a, const Meta& m, int d, const void* p, uint64_t n) {
+__device__ __forceinline__ bool store_ok(const PrepArgs& a, const DevDstPtr& dp, const void* p, uint64_t n) {
   if (!kDebug) return true;
-  const DevDstPtr& dp = a.dst_ptrs[m.dst_begin + d];
   const uint8_t* q = static_cast<const uint8_t*>(p);
   if (q >= dp.pool_begin && q + n <= dp.pool_end) return true;
-  atomicExch(a.error_word, 1);
+  atomicOr(a.error_word, kErrBadStore);
   return false;
 }
 
-// Issue the loads of a unit's block into v. Blocks whose rows span several
-// shards first resolve each row's address into shared memory (barrier).
-__device__ __forceinline__ void load_unit(const PrepArgs& a, const Meta& m, uint4 (&v)[kRowsPerThread],
-                                          const uint16_t** s_rowptr, int tid, int cc, int rsub) {
-  const int nrows = m.nrows(), ncols = m.ncols();
-  const uint32_t f = m.flags();
-  const int64_t N = m.N;
-  const bool vec = f & kUnitVec;
-  if (f & kUnitMulti) {
-    // row gather over several runs (the full_tensor() stand-in)
-    if (tid < kTile) {
-      const uint16_t* ptr = nullptr;
-      if (tid < nrows) {
-        const int64_t fr = (int64_t)m.bi * kTile + tid;
-        int k = a.trow_first_run[m.gtr];
-        while (fr >= a.runs[k].row0 + a.runs[k].rows) ++k;
-        const DevRun run = a.runs[k];
-        ptr = a.shard_ptrs[run.slot] + (fr - run.row0) * N;
-      }
-      s_rowptr[tid] = ptr;
-    }
-    __syncthreads();
+template <bool kDebug>
+__device__ __forceinline__ DevDstPtr load_dst(const PrepArgs& a, uint32_t i) {
+  const uint32_t* p = reinterpret_cast<const uint32_t*>(a.dst_ptrs + i);
+  DevDstPtr d;
+  d.data = reinterpret_cast<uint8_t*>(((uint64_t)ld_nc_u32(p + 1) << 32) | ld_nc_u32(p));
+  d.scale = reinterpret_cast<float*>(((uint64_t)ld_nc_u32(p + 3) << 32) | ld_nc_u32(p + 2));
+  d.pool_begin = d.pool_end = nullptr;
+  if (kDebug) {
+    d.pool_begin = reinterpret_cast<const uint8_t*>(((uint64_t)ld_nc_u32(p + 5) << 32) | ld_nc_u32(p + 4));
+    d.pool_end = reinterpret_cast<const uint8_t*>(((uint64_t)ld_nc_u32(p + 7) << 32) | ld_nc_u32(p + 6));
   }
-  const int64_t col = (int64_t)m.bj * kTile + cc * 8;
-  const uint16_t* base = m.src + (int64_t)rsub * N + col;
-  const int64_t rstep = 16 * N;
-  if (vec) {
-    const bool col_ok = cc * 8 < ncols;
+  return d;
+}
+
+// Rows that are not 16-byte aligned: the group gathers the block element by
+// element into the stage (zeros outside the block), warp w taking rows
+// w, w + 4, ..., lanes taking consecutive columns.
+__device__ void gather_stage(const PrepArgs& a, const DevUnit& m, uint8_t* sp, int wg, int lane) {
+  const int nrows = (int)(m.shape & 0xFFu) + 1, ncols = (int)((m.shape >> 8) & 0xFFu) + 1;
+  const int64_t N = m.cols;
+  int run = (int)m.src;
+  for (int r = wg; r < kTile; r += kGroupWarps) {
+    const uint16_t* row = nullptr;
+    if (r < nrows) {
+      const int64_t fr = (int64_t)m.src_row + r;
+      while (fr >= a.runs[run].row0 + a.runs[run].rows) ++run;
+      const DevRun rn = a.runs[run];
+      row = a.shard_ptrs[rn.slot] + (fr - rn.row0) * N + (int64_t)m.bj * kTile;
+    }
+    uint16_t* out = reinterpret_cast<uint16_t*>(sp + r * kRowBytes);
+    for (int c = lane; c < kTile; c += 32) out[c] = (row && c < ncols) ? ld_nc_u16(row + c) : (uint16_t)0;
+  }
+}
+
+// fl32(x / s) from r = RN(1/s): one correction step (see the header),
+// written with t = -e so that x = -0 gives -0 (-0 + -0), not +0.
+__device__ __forceinline__ float quotient(float x, float s, float r) {
+  const float q0 = __fmul_rn(x, r);
+  const float t = __fmaf_rn(q0, s, -x);
+  return __fmaf_rn(t, -r, q0);
+}
+
+// 8 BF16 elements (one 16-byte chunk) -> 8 codes by the correction step.
+__device__ __forceinline__ uint2 quant_chunk(const uint4& v, float s, float r) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  uint32_t c[4];
 #pragma unroll
-    for (int i = 0; i < kRowsPerThread; ++i) {
-      const int r = rsub + 16 * i;
-      v[i] = make_uint4(0, 0, 0, 0);
-      if (r < nrows && col_ok) {
-        const uint16_t* p = (f & kUnitMulti) ? s_rowptr[r] + col : base + i * rstep;
-        v[i] = ld_stream_v4(p);
+  for (int k = 0; k < 4; ++k) c[k] = e4m3x2(quotient(bf16_lo(w[k]), s, r), quotient(bf16_hi(w[k]), s, r));
+  return make_uint2(__byte_perm(c[0], c[1], 0x5410), __byte_perm(c[2], c[3], 0x5410));
+}
+
+// 8 BF16 elements (one 16-byte chunk) -> 8 codes with the IEEE division.
+__device__ __forceinline__ uint2 quant_exact(const uint4& v, float s) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  uint32_t c[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) c[k] = e4m3x2(__fdiv_rn(bf16_lo(w[k]), s), __fdiv_rn(bf16_hi(w[k]), s));
+  return make_uint2(__byte_perm(c[0], c[1], 0x5410), __byte_perm(c[2], c[3], 0x5410));
+}
+
+// Codes of one row chunk, byte by byte (outputs whose rows are not 8-byte
+// aligned); `valid` bytes of the 8 are inside the block.
+template <bool kDebug>
+__device__ __forceinline__ void store_codes_bytes(const PrepArgs& a, const DevDstPtr& dp, uint8_t* p, uint2 q,
+                                                  bool row_ok, int valid) {
+  const uint32_t wds[2] = {q.x, q.y};
+#pragma unroll
+  for (int e = 0; e < 8; ++e)
+    if (row_ok && e < valid && store_ok<kDebug>(a, dp, p + e, 1)) p[e] = (uint8_t)(wds[e >> 2] >> (8 * (e & 3)));
+}
+
+// The general FP8 path (partial blocks, rows that are not 16-byte aligned,
+// several destinations, a scale outside the correction step's range, debug
+// checks): the thread's rows again from the stage, one row at a time, to
+// every destination.
+template <bool kDebug>
+__device__ __noinline__ void store_fp8_general(const PrepArgs& a, const DevUnit m, const DevDstPtr dp0,
+                                               const uint8_t* tp, float s, int t, int r0, int cc,
+                                               int64_t row_off, int64_t row_step) {
+  const int nrows = (int)(m.shape & 0xFFu) + 1, ncols = (int)((m.shape >> 8) & 0xFFu) + 1;
+  const bool vec = (m.shape >> 16) & kUnitVec;
+  const uint32_t se = (__float_as_uint(s) >> 23) & 0xFFu;
+  const bool corr = se >= kMinScaleExp && se <= kMaxScaleExp;
+  const float r = corr ? __frcp_rn(s) : 0.0f;
+  const uint32_t tiles_n = (m.cols + kTile - 1) / kTile;
+  for (uint32_t d = 0; d < m.num_dsts; ++d) {
+    const DevDstPtr dp = d == 0 ? dp0 : load_dst<kDebug>(a, m.dst_begin + d);
+    if (t == 0) {
+      float* sp4 = dp.scale + (uint64_t)m.bi * tiles_n + m.bj;
+      if (store_ok<kDebug>(a, dp, sp4, 4)) *sp4 = s;
+    }
+    if (cc * 8 >= ncols) continue;
+    uint8_t* row = dp.data + row_off;
+#pragma unroll 1
+    for (int j = 0; j < kRows && r0 + kRowStride * j < nrows; ++j) {
+      const uint4 v = *reinterpret_cast<const uint4*>(tp + j * kRowStride * kRowBytes);
+      const uint2 q = corr ? quant_chunk(v, s, r) : quant_exact(v, s);
+      uint8_t* p = row + j * row_step;
+      if (vec) {
+        if (store_ok<kDebug>(a, dp, p, 8)) *reinterpret_cast<uint2*>(p) = q;
+      } else {
+        store_codes_bytes<kDebug>(a, dp, p, q, true, ncols - cc * 8);
       }
     }
-  } else {
+  }
+}
+
+// The general BF16 pass-through path, same cases.
+template <bool kDebug>
+__device__ __noinline__ void store_bf16_general(const PrepArgs& a, const DevUnit m, const DevDstPtr dp0,
+                                                const uint8_t* tp, int r0, int cc, int64_t row_off,
+                                                int64_t row_step) {
+  const int nrows = (int)(m.shape & 0xFFu) + 1, ncols = (int)((m.shape >> 8) & 0xFFu) + 1;
+  const bool vec = (m.shape >> 16) & kUnitVec;
+  if (cc * 8 >= ncols) return;
+  for (uint32_t d = 0; d < m.num_dsts; ++d) {
+    const DevDstPtr dp = d == 0 ? dp0 : load_dst<kDebug>(a, m.dst_begin + d);
+    uint8_t* row = dp.data + 2 * row_off;
+#pragma unroll 1
+    for (int j = 0; j < kRows && r0 + kRowStride * j < nrows; ++j) {
+      const uint4 v = *reinterpret_cast<const uint4*>(tp + j * kRowStride * kRowBytes);
+      uint8_t* p = row + 2 * j * row_step;
+      if (vec) {
+        if (store_ok<kDebug>(a, dp, p, 16)) *reinterpret_cast<uint4*>(p) = v;
+      } else {
+        const uint32_t wds[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-    for (int i = 0; i < kRowsPerThread; ++i) {
-      const int r = rsub + 16 * i;
-      uint16_t e[8];
-      const uint16_t* p = nullptr;
-      if (r < nrows) p = (f & kUnitMulti) ? s_rowptr[r] + col : base + i * rstep;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        e[j] = 0;
-        if (r < nrows && cc * 8 + j < ncols) e[j] = ld_stream_u16(p + j);
+        for (int e = 0; e < 8; ++e)
+          if (cc * 8 + e < ncols && store_ok<kDebug>(a, dp, p + 2 * e, 2))
+            *reinterpret_cast<uint16_t*>(p + 2 * e) = (uint16_t)(wds[e >> 1] >> (16 * (e & 1)));
       }
-      v[i] = make_uint4(e[0] | ((uint32_t)e[1] << 16), e[2] | ((uint32_t)e[3] << 16),
-                        e[4] | ((uint32_t)e[5] << 16), e[6] | ((uint32_t)e[7] << 16));
     }
   }
 }
 
 template <bool kDebug>
-__device__ __forceinline__ void store_fp8(const PrepArgs& a, const Meta& m,
-                                          const uint2 (&q)[kRowsPerThread], float s, int tid,
-                                          int cc, int rsub) {
-  const int nrows = m.nrows(), ncols = m.ncols();
-  const int64_t N = m.N;
-  const bool vec = m.flags() & kUnitVec;
-  const int64_t off0 = ((int64_t)m.bi * kTile + rsub) * N + (int64_t)m.bj * kTile + cc * 8;
-  const int64_t rstep = 16 * N;
-  const uint32_t tiles_n = (m.N + kTile - 1) / kTile;
-  for (int d = 0; d < (int)m.num_dsts; ++d) {
-    uint8_t* data = m.dst0;
-    float* scale = m.scale0;
-    if (d > 0) {
-      const DevDstPtr dp = a.dst_ptrs[m.dst_begin + d];
-      data = dp.data;
-      scale = dp.scale;
+__device__ void consumer(const PrepArgs& a, SmemCtl& sm, uint8_t* stages, int64_t n_local, int g, int t) {
+  const int lane = t & 31, wg = t >> 5;
+  const int cc = t & 15;       // 16-byte column chunk
+  const int r0 = t >> 4;       // first row; rows r0 + kRowStride j
+  const int bar_id = 1 + g;
+  int it = 0;
+  for (int64_t k = g; k < n_local; k += kGroups, ++it) {
+    const int st = (int)(k % kStages);
+    const bool ok = wait_bounded(smem_u32(&sm.full[st]), (uint32_t)((k / kStages) & 1), a.timeout_ns,
+                                 &sm.abort_flag);
+    if (!ok) give_up(a, sm);
+    if (bar_red_or(bar_id, kGroupThreads, !ok)) return;
+    DevUnit m;
+    {
+      const uint4 m0 = reinterpret_cast<const uint4*>(&sm.meta[st])[0];
+      const uint4 m1 = reinterpret_cast<const uint4*>(&sm.meta[st])[1];
+      m = DevUnit{m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
     }
-    if (tid == 0) {
-      float* sp = scale + (uint64_t)m.bi * tiles_n + m.bj;
-      if (store_ok<kDebug>(a, m, d, sp, 4)) *sp = s;
+    const DevDstPtr dp0 = load_dst<kDebug>(a, m.dst_begin);
+    const uint32_t flags = m.shape >> 16;
+    const int nrows = (int)(m.shape & 0xFFu) + 1, ncols = (int)((m.shape >> 8) & 0xFFu) + 1;
+    const bool whole = (m.shape & 0xFFFFu) == 0x7F7Fu;
+    const bool vec = flags & kUnitVec;
+    uint8_t* sp = stages + (size_t)st * kStageBytes;
+    if (!vec) {
+      gather_stage(a, m, sp, wg, lane);
+      fence_proxy_async_smem();          // the stage is refilled by copies later
+      bar_sync(bar_id, kGroupThreads);
     }
-    uint8_t* row = data + off0;
-    if (vec) {
-      const bool col_ok = cc * 8 < ncols;
+    uint4 v[kRows];
+    const uint8_t* tp = sp + r0 * kRowBytes + cc * 16;
+    if (whole) {
 #pragma unroll
-      for (int i = 0; i < kRowsPerThread; ++i) {
-        uint8_t* p = row + i * rstep;
-        if (rsub + 16 * i < nrows && col_ok && store_ok<kDebug>(a, m, d, p, 8))
-          *reinterpret_cast<uint2*>(p) = q[i];
-      }
+      for (int j = 0; j < kRows; ++j) v[j] = *reinterpret_cast<const uint4*>(tp + j * kRowStride * kRowBytes);
     } else {
 #pragma unroll
-      for (int i = 0; i < kRowsPerThread; ++i) {
-        const uint32_t wds[2] = {q[i].x, q[i].y};
-        uint8_t* p = row + i * rstep;
-#pragma unroll
-        for (int j = 0; j < 8; ++j)
-          if (rsub + 16 * i < nrows && cc * 8 + j < ncols && store_ok<kDebug>(a, m, d, p + j, 1))
-            p[j] = (uint8_t)(wds[j >> 2] >> (8 * (j & 3)));
+      for (int j = 0; j < kRows; ++j) {
+        v[j] = make_uint4(0, 0, 0, 0);
+        if (r0 + kRowStride * j < nrows && cc * 8 < ncols)
+          v[j] = *reinterpret_cast<const uint4*>(tp + j * kRowStride * kRowBytes);
       }
     }
-  }
-}
+    const int64_t N = m.cols;
+    const int64_t row_off = ((int64_t)m.bi * kTile + r0) * N + (int64_t)m.bj * kTile + cc * 8;
+    const int64_t row_step = kRowStride * N;
 
-template <bool kDebug>
-__device__ __forceinline__ void store_bf16(const PrepArgs& a, const Meta& m,
-                                           const uint4 (&v)[kRowsPerThread], int cc, int rsub) {
-  const int nrows = m.nrows(), ncols = m.ncols();
-  const int64_t N = m.N;
-  const bool vec = m.flags() & kUnitVec;
-  const int64_t off0 = 2 * (((int64_t)m.bi * kTile + rsub) * N + (int64_t)m.bj * kTile + cc * 8);
-  const int64_t rstep = 32 * N;
-  for (int d = 0; d < (int)m.num_dsts; ++d) {
-    uint8_t* data = d == 0 ? m.dst0 : a.dst_ptrs[m.dst_begin + d].data;
-    uint8_t* row = data + off0;
-    if (vec) {
-      const bool col_ok = cc * 8 < ncols;
-#pragma unroll
-      for (int i = 0; i < kRowsPerThread; ++i) {
-        uint8_t* p = row + i * rstep;
-        if (rsub + 16 * i < nrows && col_ok && store_ok<kDebug>(a, m, d, p, 16))
-          *reinterpret_cast<uint4*>(p) = v[i];
-      }
-    } else {
-#pragma unroll
-      for (int i = 0; i < kRowsPerThread; ++i) {
-        const uint32_t wds[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
-        uint8_t* p = row + i * rstep;
-#pragma unroll
-        for (int j = 0; j < 8; ++j)
-          if (rsub + 16 * i < nrows && cc * 8 + j < ncols && store_ok<kDebug>(a, m, d, p + 2 * j, 2))
-            *reinterpret_cast<uint16_t*>(p + 2 * j) = (uint16_t)(wds[j >> 1] >> (16 * (j & 1)));
-      }
-    }
-  }
-}
+    // the common case runs straight through: a whole block of 16-byte rows
+    // with one destination; everything else takes the general routines
+    const bool fast = !kDebug && whole && vec && m.num_dsts == 1;
+    const uint32_t empty = smem_u32(&sm.empty[st]);
 
-template <bool kDebug>
-__global__ void __launch_bounds__(kThreads, 3) prep_kernel(const PrepArgs a) {
-  __shared__ __align__(16) uint32_t s_meta[kMetaSlots][kMetaWords];
-  __shared__ const uint16_t* s_rowptr[kTile];
-  __shared__ float s_wmax[2][kWarps];
-  const int tid = threadIdx.x;
-  const int lane = tid & 31, warp = tid >> 5;
-  const int cc = tid & 15;            // 16-byte column chunk within the block
-  const int rsub = tid >> 4;          // first row within the block
-  const int64_t G = gridDim.x;
-
-  int64_t u = a.unit_begin + blockIdx.x;
-  if (u >= a.unit_end) return;
-  // descriptor words (lanes 0..7 of warp 0) of the units one and two ahead
-  uint32_t wa = 0, wb = 0;
-  if (warp == 0) {
-    const uint32_t w0 = fetch_unit_word(a, u, lane);
-    const uint32_t d0 = fetch_dyn_word(a, w0, lane, true);
-    if (lane < 14) s_meta[0][lane] = lane < 8 ? w0 : d0;
-    wa = fetch_unit_word(a, u + G, lane);
-    wb = fetch_unit_word(a, u + 2 * G, lane);
-  }
-  __syncthreads();
-  uint4 v[kRowsPerThread];
-  load_unit(a, read_meta(s_meta[0]), v, s_rowptr, tid, cc, rsub);
-
-  for (int n = 0;; ++n) {
-    const int slot = n & (kMetaSlots - 1), nslot = (n + 1) & (kMetaSlots - 1);
-    const int buf = n & 1;
-    const int64_t un = u + G;
-    const bool has_next = un < a.unit_end;
-    uint32_t dn = 0;
-    if (warp == 0) dn = fetch_dyn_word(a, wa, lane, has_next);
-    const uint32_t flags = s_meta[slot][5] >> 16;
     if (flags & kUnitFp8) {
-      // block amax: per thread, then warp shuffle, then across warps
-      uint32_t m2 = 0;
+      // block amax: per thread, across the warp, across the group's warps
+      uint32_t a0 = 0, a1 = 0, a2 = 0, a3 = 0;
 #pragma unroll
-      for (int i = 0; i < kRowsPerThread; ++i) {
-        m2 = absmax_bf16x2(m2, v[i].x);
-        m2 = absmax_bf16x2(m2, v[i].y);
-        m2 = absmax_bf16x2(m2, v[i].z);
-        m2 = absmax_bf16x2(m2, v[i].w);
+      for (int j = 0; j < kRows; ++j) {
+        a0 = absmax_bf16x2(a0, v[j].x);
+        a1 = absmax_bf16x2(a1, v[j].y);
+        a2 = absmax_bf16x2(a2, v[j].z);
+        a3 = absmax_bf16x2(a3, v[j].w);
       }
-      m2 &= 0x7FFF7FFFu;
+      const uint32_t m2 = absmax_bf16x2(absmax_bf16x2(a0, a1), absmax_bf16x2(a2, a3)) & 0x7FFF7FFFu;
       float mx = fmaxf(bf16_lo(m2), bf16_hi(m2));
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, off));
-      if (warp == 0) {
-        if (lane < 14) s_meta[nslot][lane] = lane < 8 ? wa : dn;
-        wa = wb;
-        wb = fetch_unit_word(a, un + 2 * G, lane);
-      }
-      if (lane == 0) s_wmax[buf][warp] = mx;
-      __syncthreads();
-      float amax = s_wmax[buf][0];
+      if (lane == 0) sm.wmax[g][it & 1][wg] = mx;
+      bar_sync(bar_id, kGroupThreads);
+      const float* wm = sm.wmax[g][it & 1];
+      float amax = wm[0];
 #pragma unroll
-      for (int w = 1; w < kWarps; ++w) amax = fmaxf(amax, s_wmax[buf][w]);
+      for (int w = 1; w < kGroupWarps; ++w) amax = fmaxf(amax, wm[w]);
       const float s = amax == 0.0f ? 1.0f : __fdiv_rn(amax, 448.0f);
       const uint32_t se = (__float_as_uint(s) >> 23) & 0xFFu;
-      uint2 q[kRowsPerThread];
-      if (se >= 1u && se <= 252u) {           // s and 1/s normal: bracketed path
+      if (fast && se >= kMinScaleExp && se <= kMaxScaleExp) {
         const float r = __frcp_rn(s);
-        const float rlo = r * (1.0f - 0x1p-21f), rhi = r * (1.0f + 0x1p-21f);
+        uint2 q[kRows];
 #pragma unroll
-        for (int i = 0; i < kRowsPerThread; ++i)
-          if (!quant_chunk_bracket(v[i], rlo, rhi, q[i])) q[i] = quant_chunk_exact(v[i], s);
+        for (int j = 0; j < kRows; ++j) q[j] = quant_chunk(v[j], s, r);
+        mbar_arrive(empty);                       // the codes are in registers
+        if (t == 0) dp0.scale[(uint64_t)m.bi * ((m.cols + kTile - 1) / kTile) + m.bj] = s;
+        uint8_t* row = dp0.data + row_off;
+#pragma unroll
+        for (int j = 0; j < kRows; ++j) *reinterpret_cast<uint2*>(row + j * row_step) = q[j];
       } else {
+        store_fp8_general<kDebug>(a, m, dp0, tp, s, t, r0, cc, row_off, row_step);
+        mbar_arrive(empty);
+      }
+    } else if (fast) {
+      mbar_arrive(empty);                         // the block is in registers
+      uint8_t* row = dp0.data + 2 * row_off;
 #pragma unroll
-        for (int i = 0; i < kRowsPerThread; ++i) q[i] = quant_chunk_exact(v[i], s);
-      }
-      if (has_next) load_unit(a, read_meta(s_meta[nslot]), v, s_rowptr, tid, cc, rsub);
-      store_fp8<kDebug>(a, read_meta(s_meta[slot]), q, s, tid, cc, rsub);
+      for (int j = 0; j < kRows; ++j) *reinterpret_cast<uint4*>(row + 2 * j * row_step) = v[j];
     } else {
-      if (warp == 0) {
-        if (lane < 14) s_meta[nslot][lane] = lane < 8 ? wa : dn;
-        wa = wb;
-        wb = fetch_unit_word(a, un + 2 * G, lane);
-      }
-      __syncthreads();
-      store_bf16<kDebug>(a, read_meta(s_meta[slot]), v, cc, rsub);
-      if (has_next) load_unit(a, read_meta(s_meta[nslot]), v, s_rowptr, tid, cc, rsub);
+      store_bf16_general<kDebug>(a, m, dp0, tp, r0, cc, row_off, row_step);
+      mbar_arrive(empty);
     }
-    if (!has_next) break;
-    u = un;
   }
+}
+
+template <bool kDebug>
+__global__ void __launch_bounds__(kCtaThreads, 1) prep_kernel(const __grid_constant__ PrepArgs a) {
+  extern __shared__ unsigned char smem_raw[];
+  uint8_t* stages = reinterpret_cast<uint8_t*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  SmemCtl& sm = *reinterpret_cast<SmemCtl*>(stages + (size_t)kStages * kStageBytes);
+  const int tid = threadIdx.x;
+  const int64_t first = a.unit_begin + blockIdx.x;
+  const int64_t n_local = first < a.unit_end ? (a.unit_end - first + gridDim.x - 1) / gridDim.x : 0;
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(smem_u32(&sm.full[s]), 1);
+      mbar_init(smem_u32(&sm.empty[s]), kGroupThreads);
+    }
+    sm.abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  if (n_local == 0) return;
+  if (tid >= kConsumerThreads)
+    producer(a, sm, smem_u32(stages), first, n_local, tid & 31);
+  else
+    consumer<kDebug>(a, sm, stages, n_local, tid / kGroupThreads, tid % kGroupThreads);
 }
 
 }  // namespace
 
-int prep_blocks_per_sm() {
-  int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, prep_kernel<false>, kThreads, 0) != cudaSuccess)
-    return 1;
-  return n > 0 ? n : 1;
+cudaError_t prep_kernel_setup() {
+  cudaError_t e = cudaFuncSetAttribute(prep_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)kSmemBytes);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(prep_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)kSmemBytes);
 }
 
 cudaError_t launch_prepare(const PrepArgs& a, int grid, cudaStream_t s, bool debug) {
   if (a.unit_end <= a.unit_begin) return cudaSuccess;
   if (debug)
-    prep_kernel<true><<<grid, kThreads, 0, s>>>(a);
+    prep_kernel<true><<<grid, kCtaThreads, kSmemBytes, s>>>(a);
   else
-    prep_kernel<false><<<grid, kThreads, 0, s>>>(a);
+    prep_kernel<false><<<grid, kCtaThreads, kSmemBytes, s>>>(a);
   return cudaGetLastError();
 }
 

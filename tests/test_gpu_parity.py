@@ -47,15 +47,20 @@ def test_edge_stress_full(oracle_mod):
 
 def test_small_shapes_and_special_values(oracle_mod):
     """1x1, 3x5, 129x130 fused, 256x1, shards of 0 and 1 rows, -0.0 blocks,
-    subnormal scales, outliers, replicated destinations on two ranks."""
+    subnormal scales, outliers, replicated destinations on two ranks; 64-column
+    outputs narrower than one block (FP8 from two shards, BF16 from one) and a
+    fused BF16 output whose partial blocks span three shards."""
     params = [Param("a", 1, 1, (1,)), Param("b", 3, 5, (2, 0, 1)),
               Param("c1", 50, 130, (17, 33)), Param("c2", 79, 130, (1, 0, 40, 38)),
               Param("d", 256, 1, (100, 100, 56)), Param("e", 300, 264, (1,) * 44 + (256,)),
-              Param("negzero", 130, 136, (130,)), Param("tiny", 128, 128, (128,))]
+              Param("negzero", 130, 136, (130,)), Param("tiny", 128, 128, (128,)),
+              Param("f", 40, 64, (17, 23)), Param("g", 200, 64, (200,)),
+              Param("h1", 70, 72, (70,)), Param("h2", 90, 72, (0, 45, 45))]
     outs = [Output("a", (0,), True, (0,)), Output("b", (1,), True, (1, 0)),
             Output("c", (2, 3), True, (1,)), Output("d", (4,), False, (0, 1)),
             Output("e", (5,), True, (0, 1)), Output("negzero", (6,), True, (0,)),
-            Output("tiny", (7,), True, (1,))]
+            Output("tiny", (7,), True, (1,)), Output("f", (8,), True, (0,)),
+            Output("g", (9,), False, (1,)), Output("h", (10, 11), False, (0, 1))]
     w = Workload("small", params, outs, 2, ValueRecipe("student_t3", 0.02, 77))
     shards = make_shards(w, device="cuda:0")
     shards[6] = [torch.full((130, 136), -0.0, dtype=torch.bfloat16, device="cuda:0")]
