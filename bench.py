@@ -36,9 +36,11 @@ GiB = 1 << 30
 SPEC_HBM_GBS = 8000.0
 
 # dram__bytes_read.sum + dram__bytes_write.sum of one prep_kernel launch,
-# from the ncu capture summarised in profiles/, scaled to the full layer;
-# valid only for the kernel source it was taken on.
-TRAFFIC = {"kernel_sha256": None, "bytes_per_launch": None}
+# from the ncu capture summarised in profiles/ (16 experts, scaled by the
+# blocks processed to the 385-expert layer); valid only for the kernel
+# source it was taken on.
+TRAFFIC = {"kernel_sha256": "856b1f00a7b721ce20baefa848a5806f2c533a4dd6359618b9932770afd21035",
+           "bytes_per_launch": 49553109375, "experts": 385}
 
 
 def kernel_sha() -> str:
@@ -271,7 +273,8 @@ def main():
     peaks = measured_peaks()
     peak = peaks.get("hbm_gbs")
     achieved = alg_bytes / avg_launch_s / 1e9
-    traffic = TRAFFIC["bytes_per_launch"] if TRAFFIC["kernel_sha256"] == kernel_sha() else None
+    traffic = (TRAFFIC["bytes_per_launch"]
+               if TRAFFIC["kernel_sha256"] == kernel_sha() and TRAFFIC["experts"] == args.experts else None)
     roofline = {"bound": "hbm", "achieved": round(achieved, 1),
                 "peak": peak if peak else 6400.0, "unit": "GB/s",
                 "frac": round(achieved / (peak if peak else 6400.0), 4),
