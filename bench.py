@@ -39,8 +39,8 @@ SPEC_HBM_GBS = 8000.0
 # from the ncu capture summarised in profiles/ (16 experts, scaled by the
 # blocks processed to the 385-expert layer); valid only for the kernel
 # source it was taken on.
-TRAFFIC = {"kernel_sha256": "856b1f00a7b721ce20baefa848a5806f2c533a4dd6359618b9932770afd21035",
-           "bytes_per_launch": 49553109375, "experts": 385}
+TRAFFIC = {"kernel_sha256": "212e5daff6154098a833a55a2de9df34ca96e836d1ce7cd1e36f4c9bf673e160",
+           "bytes_per_launch": 49545488300, "experts": 385}
 
 
 def kernel_sha() -> str:

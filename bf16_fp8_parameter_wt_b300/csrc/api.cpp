@@ -324,6 +324,8 @@ wt_status wt_prepare(wt_plan* h, const void* const* shard_ptrs, void* const* poo
   PrepArgs a = p.args;
   a.shard_ptrs = p.d_shard_ptrs;
   a.tmaps = p.d_tmaps;
+  a.stall_unit = p.stall_unit;
+  a.timeout_ns = p.wait_limit_ns ? p.wait_limit_ns : kDefaultTimeoutNs;
   a.tmap_fence = p.tmaps_dirty ? 1u : 0u;
   a.unit_begin = 0;
   a.unit_end = p.num_units;
@@ -352,6 +354,8 @@ wt_status wt_prepare_offload(wt_plan* h, const void* host_image, void* const* po
   PrepArgs a = p.args;
   a.shard_ptrs = p.d_offload_shard_ptrs;
   a.tmaps = p.d_offload_tmaps;
+  a.stall_unit = p.stall_unit;
+  a.timeout_ns = p.wait_limit_ns ? p.wait_limit_ns : kDefaultTimeoutNs;
   const char* host = static_cast<const char*>(host_image);
   auto drain = [&](wt_status s_, const std::string& msg) {
     cudaStreamSynchronize(cs);
@@ -412,6 +416,14 @@ wt_status wt_plan_check(wt_plan* h, void* stream) {
 wt_status wt_debug_fail_offload_chunk(wt_plan* h, int32_t chunk) {
   if (!h) return fail(WT_ERR_INVALID_ARGUMENT, "plan is NULL");
   h->p.fail_chunk = chunk;
+  return WT_OK;
+}
+
+wt_status wt_debug_stall_unit(wt_plan* h, int64_t unit, uint64_t wait_limit_ns) {
+  if (!h) return fail(WT_ERR_INVALID_ARGUMENT, "plan is NULL");
+  if (unit < -1 || unit >= h->p.num_units) return fail(WT_ERR_INVALID_ARGUMENT, "unit out of range");
+  h->p.stall_unit = unit;
+  h->p.wait_limit_ns = wait_limit_ns;
   return WT_OK;
 }
 

@@ -74,6 +74,7 @@ struct PrepArgs {
   int32_t* error_word;               // kErr* bits
   uint64_t timeout_ns;               // limit of every wait inside the kernel
   uint32_t tmap_fence;               // tensor maps were rewritten since the last launch
+  int64_t stall_unit;                // testing: this unit is never filled (-1: none)
 };
 
 // Host-side copy of one param.
@@ -164,6 +165,9 @@ struct Plan {
   cudaEvent_t prep_done[2] = {nullptr, nullptr};
   bool prep_recorded[2] = {false, false};
   int32_t fail_chunk = -1;
+  // testing hooks (wt_debug_stall_unit)
+  int64_t stall_unit = -1;
+  uint64_t wait_limit_ns = 0;        // 0: kDefaultTimeoutNs
 };
 
 // plan.cpp

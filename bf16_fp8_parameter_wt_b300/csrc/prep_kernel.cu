@@ -265,6 +265,9 @@ __device__ void producer(const PrepArgs& a, SmemCtl& sm, uint32_t stage0, int64_
         ok = false;
         break;
       }
+      // testing hook: leave this unit's stage unfilled, so that its
+      // consumers' wait runs out
+      if (first + k * (int64_t)gridDim.x == a.stall_unit) continue;
       const uint32_t flags = w[5] >> 16;
       const uint32_t dst = stage0 + (uint32_t)st * kStageBytes;
       if (lane == 0) {

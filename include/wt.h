@@ -217,16 +217,29 @@ wt_status wt_prepare_offload(wt_plan* p, const void* host_image,
 wt_status wt_prepare_noalloc(const wt_plan_desc* desc, const void* const* shard_ptrs,
                              void* const* pools, void* stream);
 
-/* With WT_FLAG_DEBUG_CHECKS: synchronise `stream`, then report
- * WT_ERR_INTERNAL if any store of an earlier wt_prepare* fell outside its
- * destination range (the offending store is skipped, never performed), and
- * clear the flag. Without the flag: WT_OK after the synchronisation. */
+/* Synchronise `stream`, then report what the kernels of earlier
+ * wt_prepare* calls recorded, and clear it: WT_ERR_TIMEOUT if a wait inside
+ * the kernel gave up (every wait is bounded; the step's output is then
+ * incomplete), else, with WT_FLAG_DEBUG_CHECKS, WT_ERR_INTERNAL if a store
+ * fell outside its destination range (the offending store is skipped,
+ * never performed). WT_OK otherwise. */
 wt_status wt_plan_check(wt_plan* p, void* stream);
 
 /* Testing hook: make chunk `chunk` of the next wt_prepare_offload calls
  * fail on the host before it is queued (-1 disables). Exercises the
  * drain-and-report path without touching the GPU. */
 wt_status wt_debug_fail_offload_chunk(wt_plan* p, int32_t chunk);
+
+/* Testing hook for the kernel's bounded waits: the next wt_prepare* calls
+ * on this plan never fill the shared-memory stage of work unit `unit`
+ * (a 128x128 block, numbered over all outputs in plan order), and every
+ * wait inside the kernel gives up after wait_limit_ns (0 = the default of
+ * 2 s). The consumers of that stage then stop waiting, the kernel records
+ * the timeout, waits (bounded) for its copies in flight, and returns; the
+ * next wt_plan_check reports WT_ERR_TIMEOUT and the pools hold an
+ * incomplete step. Nothing faults or hangs, and the plan stays usable.
+ * unit = -1 restores normal operation. Errors: WT_ERR_INVALID_ARGUMENT. */
+wt_status wt_debug_stall_unit(wt_plan* p, int64_t unit, uint64_t wait_limit_ns);
 
 /* Synchronise the plan's device with the last stream it ran on, then free
  * the plan and everything it owns. NULL is accepted. */

@@ -153,3 +153,17 @@ def test_null_arguments():
     assert L.wt_plan_pool_bytes(None, 0, None) == 1
     assert L.wt_prepare(None, None, None, None) == 1
     assert L.wt_plan_destroy(None) == 0
+
+
+def test_testing_hooks_validate_their_arguments():
+    L = wt.lib()
+    assert L.wt_debug_stall_unit(None, 0, 0) == 1
+    assert L.wt_debug_fail_offload_chunk(None, 0) == 1
+    with wt.Plan(_simple(), device=-1) as p:
+        n = p.stats["num_units"]
+        for bad in (-2, n):
+            with pytest.raises(wt.WTError) as ei:
+                wt.wt_debug_stall_unit(p.handle, bad, 0)
+            assert ei.value.name == "WT_ERR_INVALID_ARGUMENT"
+        wt.wt_debug_stall_unit(p.handle, n - 1, 1000)
+        wt.wt_debug_stall_unit(p.handle, -1, 0)
