@@ -4,15 +4,16 @@ experts + 1 shared, w1/w3 2048x7168 fused to gate_up 4096x7168, w2
 ranks; 16.96 G params, 33.9 GB BF16 read, 16.96 GB written per step).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
-                  [--workload kimi_k2_moe_layer|offload_8layer] [--no-e2e]
-                  [--no-cpu-baseline] [--experts E]
+                  [--workload kimi_k2_moe_layer|offload_8layer] [--images K]
+                  [--no-e2e] [--no-cpu-baseline] [--experts E]
 
 Prints one JSON line. `value` is GB/s of BF16 input for the whole job
 (all ranks), timed with CUDA events on the launching stream around K
 back-to-back steps whose inputs (33.9 GB) are far larger than L2. `e2e`
 is the same metric through wt_prepare_offload from pinned host memory,
-with the host-to-device copies and a device-to-host read of every
-destination pool inside the timed region. `--impl reference` times the CPU
+with the host-to-device copies and the read-back of the step's status
+inside the timed region. `--workload offload_8layer` instead times the
+8-layer streamed-offload stack (its own JSON line). `--impl reference` times the CPU
 oracle on the host cores on a bounded sample of the same workload.
 Under torchrun each rank prepares its own layer (weak scaling, no
 collective on the data path).
@@ -34,6 +35,7 @@ sys.path.insert(0, ROOT)
 METRIC = "wt_prepare GB/s (BF16 in) and params/s at 1 B300; % of HBM roofline"
 GiB = 1 << 30
 SPEC_HBM_GBS = 8000.0
+L2_BYTES = 126 * 10**6
 
 # dram__bytes_read.sum + dram__bytes_write.sum of one prep_kernel launch,
 # from the ncu capture summarised in profiles/ (16 experts, scaled by the
@@ -132,13 +134,30 @@ def max_over_ranks(world, v: float, dev) -> float:
     return float(t.item())
 
 
+def sample_outputs(w, experts: int, target_bytes: int = 700_000_000) -> list:
+    """A bounded sample of a workload's outputs: the first `experts` experts
+    of an MoE layer, else the first outputs up to about target_bytes of
+    BF16 input (at least one)."""
+    if w.name.startswith("kimi_k2_moe_layer"):
+        return list(range(min(len(w.outputs), 2 * experts)))
+    out, total = [], 0
+    for o in range(len(w.outputs)):
+        m, n = w.output_shape(o)
+        if out and total + 2 * m * n > target_bytes:
+            break
+        out.append(o)
+        total += 2 * m * n
+    return out
+
+
 def cpu_baseline(w_full, experts_sample: int, steps: int = 1) -> dict:
-    """Time the CPU oracle, as it stands, on the first `experts_sample`
-    experts of the layer (same shapes, same value recipe)."""
+    """Time the CPU oracle, as it stands, on a bounded sample of the
+    workload's outputs (same shapes, same value recipe)."""
     import oracle
     from workloads import make_shards, shards_to_host_u16
     oracle.build()
-    sub = w_full.subset(range(2 * experts_sample), name=f"{w_full.name}[:{experts_sample} experts]")
+    outs = sample_outputs(w_full, experts_sample)
+    sub = w_full.subset(outs, name=f"{w_full.name}[:{len(outs)} outputs]")
     host = shards_to_host_u16(make_shards(sub, device="cpu"))
     m = oracle.Model(sub)
     cores = max(1, len(os.sched_getaffinity(0)))
@@ -150,7 +169,7 @@ def cpu_baseline(w_full, experts_sample: int, steps: int = 1) -> dict:
     t = statistics.median(times)
     return {"value": round(sub.bytes_read / t / 1e9, 4), "unit": "GB/s", "cores": cores,
             "kind": "oracle", "params_per_s": round(sub.num_params_total / t, 1),
-            "sample": f"{experts_sample} of {len(w_full.outputs) // 2} experts "
+            "sample": f"{len(outs)} of {len(w_full.outputs)} outputs "
                       f"({sub.num_params_total} params, {sub.bytes_read} B BF16 in), "
                       f"median of {steps} run(s), {t:.2f} s each"}
 
@@ -206,6 +225,12 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--cpu-experts", type=int, default=8)
     ap.add_argument("--reference-experts", type=int, default=2)
+    ap.add_argument("--workload", default="kimi_k2_moe_layer",
+                    choices=["kimi_k2_moe_layer", "llama_dense", "edge_stress", "tiny_dense",
+                             "offload_8layer"])
+    ap.add_argument("--images", type=int, default=2)
+    ap.add_argument("--stack-steps", type=int, default=2)
+    ap.add_argument("--stack-warmup", type=int, default=1)
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -215,16 +240,22 @@ def main():
     if args.impl == "reference":
         run_reference(args, world, rank)
         return
+    if args.workload == "offload_8layer":
+        run_offload_stack(args, world, rank, local)
+        return
 
     import torch
     import bf16_fp8_parameter_wt_b300 as wt
     from bf16_fp8_parameter_wt_b300 import build as wt_build
-    from workloads import kimi_k2_moe_layer, make_shards
+    from workloads import WORKLOADS, kimi_k2_moe_layer, make_shards
 
     wt_build.build()
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    w = kimi_k2_moe_layer(args.experts, seed=1003 + rank)
+    if args.workload == "kimi_k2_moe_layer":
+        w = kimi_k2_moe_layer(args.experts, seed=1003 + rank)
+    else:
+        w = WORKLOADS[args.workload]()
     shards = make_shards(w, device=dev)
     flat = [s for per in shards for s in per]
     shard_ptrs = [s.data_ptr() for s in flat]
@@ -274,7 +305,8 @@ def main():
     peak = peaks.get("hbm_gbs")
     achieved = alg_bytes / avg_launch_s / 1e9
     traffic = (TRAFFIC["bytes_per_launch"]
-               if TRAFFIC["kernel_sha256"] == kernel_sha() and TRAFFIC["experts"] == args.experts else None)
+               if TRAFFIC["kernel_sha256"] == kernel_sha() and args.workload == "kimi_k2_moe_layer"
+               and TRAFFIC["experts"] == args.experts else None)
     roofline = {"bound": "hbm", "achieved": round(achieved, 1),
                 "peak": peak if peak else 6400.0, "unit": "GB/s",
                 "frac": round(achieved / (peak if peak else 6400.0), 4),
@@ -299,13 +331,15 @@ def main():
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
-        "data": "synthetic (seeded N(0, 0.006) BF16, generated on device)",
+        "data": f"synthetic (seeded {w.values.dist}, sigma {w.values.sigma}, BF16, generated on device)",
         "params_per_s": round(params_per_s, 1),
         "hbm_frac_of_8TBs_spec": round(value * (alg_bytes / st["bytes_read"]) / SPEC_HBM_GBS, 4),
-        "config": {"workload": w.name, "experts": args.experts, "params_per_rank": st["num_params_total"],
+        "config": {"workload": w.name, "params_per_rank": st["num_params_total"],
                    "bytes_read_per_rank": st["bytes_read"], "bytes_written_per_rank": st["bytes_written"],
-                   "io": "BF16 in; e4m3 codes + fp32 128x128 scales out",
-                   "l2": "inputs (33.9 GB) larger than L2, no flush",
+                   "io": "BF16 in; e4m3 codes + fp32 128x128 scales out (BF16 pass-through where set)",
+                   "l2": (f"inputs ({st['bytes_read'] / 1e9:.1f} GB) larger than the 126 MB L2, no flush"
+                          if st["bytes_read"] > L2_BYTES else
+                          "inputs smaller than L2: L2-resident, a latency figure"),
                    "parallelism": f"replicas x{world}" if world > 1 else "single"},
         "roofline": roofline, "e2e": e2e, "cpu_baseline": cpu, "clocks": clk,
         "gpu_launches": args.steps, "wall_s_timed": round(t_wall, 4),
@@ -318,31 +352,56 @@ def main():
         dist.destroy_process_group()
 
 
-def measure_e2e(w, shards, args, dev, world):
-    """wt_prepare_offload from a pinned host image (2 GiB chunks) plus a
-    device-to-host read of every destination pool into pinned memory."""
+def pinned_image(plan, shards):
+    """The packed pinned host image that wt_prepare_offload reads."""
     import torch
-    import bf16_fp8_parameter_wt_b300 as wt
-    plan = wt.Plan(w, device=dev.index, offload_chunk_bytes=2 * GiB)
-    st = plan.stats
-    host = torch.empty(st["host_bytes"], dtype=torch.uint8, pin_memory=True)
+    host = torch.empty(plan.stats["host_bytes"], dtype=torch.uint8, pin_memory=True)
     for p, per in enumerate(shards):
         for k, s in enumerate(per):
             off = plan.shard_host_offset(p, k)
             n = s.numel() * 2
-            host[off:off + n].copy_(s.view(torch.uint8).flatten())
+            host[off:off + n].copy_(s.reshape(-1).view(torch.uint8))
+    return host
+
+
+def h2d_peak(host, dev, stream, reps: int = 3) -> float:
+    """Best of `reps` plain pinned 2 GiB host-to-device copies (GB/s): the
+    bound of the offload path."""
+    import torch
+    n = min(2 * GiB, host.numel())
+    buf = torch.empty(n, dtype=torch.uint8, device=dev)
+    best = 0.0
+    for _ in range(reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        with torch.cuda.stream(stream):
+            buf.copy_(host[:n], non_blocking=True)
+        e1.record(stream)
+        stream.synchronize()
+        best = max(best, n / (e0.elapsed_time(e1) * 1e-3) / 1e9)
+    return best
+
+
+def measure_e2e(w, shards, args, dev, world):
+    """The same step through the public API from pinned host memory: each
+    step is wt_prepare_offload (2 GiB chunks copied host-to-device on one
+    stream while the previous chunk is prepared on another) followed by
+    wt_plan_check, which waits for the step and reads its 4-byte status
+    back to the host. The destination pools stay on the device: they stand
+    in for the remote inference memory the prepared bytes are written to."""
+    import torch
+    import bf16_fp8_parameter_wt_b300 as wt
+    plan = wt.Plan(w, device=dev.index, offload_chunk_bytes=2 * GiB)
+    st = plan.stats
+    host = pinned_image(plan, shards)
     pools = [torch.empty(max(1, plan.pool_bytes(r)), dtype=torch.uint8, device=dev)
              for r in range(w.num_ranks)]
-    host_pools = [torch.empty(p.numel(), dtype=torch.uint8, pin_memory=True) for p in pools]
     pool_ptrs = [p.data_ptr() for p in pools]
     copy_s, comp_s = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
 
     def step():
         plan.prepare_offload(host.data_ptr(), pool_ptrs, copy_s.cuda_stream, comp_s.cuda_stream)
-        with torch.cuda.stream(comp_s):
-            for hp, p in zip(host_pools, pools):
-                hp.copy_(p, non_blocking=True)
-        comp_s.synchronize()
+        plan.check(comp_s.cuda_stream)
 
     step()
     barrier(world)
@@ -351,23 +410,82 @@ def measure_e2e(w, shards, args, dev, world):
         step()
     dt = (time.perf_counter() - t0) / args.e2e_steps
     dt = max_over_ranks(world, dt, dev)
-    # one plain pinned 2 GiB host-to-device copy: the bound of this path
-    buf = torch.empty(2 * GiB, dtype=torch.uint8, device=dev)
-    best = 0.0
-    for _ in range(3):
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(copy_s)
-        with torch.cuda.stream(copy_s):
-            buf.copy_(host[:2 * GiB], non_blocking=True)
-        e1.record(copy_s)
-        copy_s.synchronize()
-        best = max(best, 2 * GiB / (e0.elapsed_time(e1) * 1e-3) / 1e9)
+    peak = h2d_peak(host, dev, copy_s)
     plan.close()
-    d2h = sum(p.numel() for p in pools)
     return {"value": round(world * st["bytes_read"] / dt / 1e9, 3), "unit": "GB/s",
-            "h2d_bytes_per_step": st["host_bytes"], "d2h_bytes_per_step": d2h,
+            "h2d_bytes_per_step": st["host_bytes"], "d2h_bytes_per_step": 4,
             "ms_per_step": round(dt * 1e3, 2), "chunks": st["num_chunks"],
-            "h2d_peak_gbs": round(best, 2), "api": "wt_prepare_offload + pool D2H"}
+            "h2d_peak_gbs": round(peak, 2),
+            "overlap_efficiency": round(st["host_bytes"] / (peak * 1e9) / dt, 4),
+            "api": "wt_prepare_offload + wt_plan_check (status read)"}
+
+
+def run_offload_stack(args, world, rank, local):
+    """The streamed-offload stack: 8 layers, each the MoE layer plus q/k/v/o
+    7168x7168 projections (qkv fused), held as BF16 shards in pinned host
+    memory and prepared through wt_prepare_offload into one set of pools
+    reused by every layer. The host holds `--images` distinct layer images
+    (seeded draws) that the 8 layers cycle through, so the pinned footprint
+    fits the host; host-to-device traffic is that of 8 distinct layers."""
+    import torch
+    import bf16_fp8_parameter_wt_b300 as wt
+    from bf16_fp8_parameter_wt_b300 import build as wt_build
+    from workloads import make_shards, offload_layer
+
+    wt_build.build()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    w = offload_layer(args.experts, seed=1005 + 100 * rank)
+    plan = wt.Plan(w, device=local, offload_chunk_bytes=2 * GiB)
+    st = plan.stats
+    images = []
+    for i in range(args.images):
+        wi = offload_layer(args.experts, seed=1005 + 100 * rank + i)
+        shards = make_shards(wi, device=dev)
+        images.append(pinned_image(plan, shards))
+        del shards
+        torch.cuda.empty_cache()
+    pools = [torch.empty(max(1, plan.pool_bytes(r)), dtype=torch.uint8, device=dev)
+             for r in range(w.num_ranks)]
+    pool_ptrs = [p.data_ptr() for p in pools]
+    copy_s, comp_s = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    layers = 8
+
+    def step():
+        for layer in range(layers):
+            plan.prepare_offload(images[layer % len(images)].data_ptr(), pool_ptrs,
+                                 copy_s.cuda_stream, comp_s.cuda_stream)
+        plan.check(comp_s.cuda_stream)
+
+    for _ in range(args.stack_warmup):
+        step()
+    barrier(world)
+    t0 = time.perf_counter()
+    for _ in range(args.stack_steps):
+        step()
+    dt = (time.perf_counter() - t0) / args.stack_steps
+    dt = max_over_ranks(world, dt, dev)
+    peak = h2d_peak(images[0], dev, copy_s)
+    plan.close()
+    host_bytes = layers * st["host_bytes"]
+    value = world * layers * st["bytes_read"] / dt / 1e9
+    line = {
+        "metric": "wt_prepare_offload GB/s (BF16 host in), 8-layer streamed offload",
+        "value": round(value, 3), "unit": "GB/s", "n_gpus": world, "steps": args.stack_steps,
+        "warmup": args.stack_warmup, "ms_per_step": round(dt * 1e3, 2), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded N(0, 0.006) BF16, pinned host images)",
+        "params_per_s": round(world * layers * st["num_params_total"] / dt, 1),
+        "config": {"workload": f"offload_stack_8x{w.name}", "layers": layers,
+                   "host_images": args.images, "chunk_bytes": 2 * GiB, "chunks_per_layer": st["num_chunks"],
+                   "parallelism": f"replicas x{world}" if world > 1 else "single"},
+        "e2e": {"value": round(value, 3), "unit": "GB/s", "h2d_bytes_per_step": host_bytes,
+                "d2h_bytes_per_step": 4},
+        "h2d_peak_gbs": round(peak, 2),
+        "overlap_efficiency": round(host_bytes / (peak * 1e9) / dt, 4),
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
 
 
 if __name__ == "__main__":

@@ -343,21 +343,47 @@ __device__ __forceinline__ DevDstPtr load_dst(const PrepArgs& a, uint32_t i) {
 
 // Rows that are not 16-byte aligned: the group gathers the block element by
 // element into the stage (zeros outside the block), warp w taking rows
-// w, w + 4, ..., lanes taking consecutive columns.
-__device__ void gather_stage(const PrepArgs& a, const DevUnit& m, uint8_t* sp, int wg, int lane) {
-  const int nrows = (int)(m.shape & 0xFFu) + 1, ncols = (int)((m.shape >> 8) & 0xFFu) + 1;
+// w, w + 4, ..., lanes taking consecutive columns. Eight rows are loaded
+// before any is stored, so 32 loads per lane are in flight; a block whose
+// rows come from one shard needs no per-row run lookup.
+__device__ __forceinline__ const uint16_t* gather_row(const PrepArgs& a, const DevUnit& m, int& run,
+                                                      const uint16_t* one_shard, int r) {
   const int64_t N = m.cols;
+  if (one_shard) return one_shard + (int64_t)r * N;
+  const int64_t fr = (int64_t)m.src_row + r;
+  while (fr >= a.runs[run].row0 + a.runs[run].rows) ++run;
+  const DevRun rn = a.runs[run];
+  return a.shard_ptrs[rn.slot] + (fr - rn.row0) * N + (int64_t)m.bj * kTile;
+}
+
+__device__ void gather_stage(const PrepArgs& a, const DevUnit& m, uint8_t* sp, int wg, int lane) {
+  constexpr int kRowsAtOnce = 8;
+  const int nrows = (int)(m.shape & 0xFFu) + 1, ncols = (int)((m.shape >> 8) & 0xFFu) + 1;
   int run = (int)m.src;
-  for (int r = wg; r < kTile; r += kGroupWarps) {
-    const uint16_t* row = nullptr;
-    if (r < nrows) {
-      const int64_t fr = (int64_t)m.src_row + r;
-      while (fr >= a.runs[run].row0 + a.runs[run].rows) ++run;
-      const DevRun rn = a.runs[run];
-      row = a.shard_ptrs[rn.slot] + (fr - rn.row0) * N + (int64_t)m.bj * kTile;
+  const uint16_t* one_shard = nullptr;
+  if (!((m.shape >> 16) & kUnitMulti)) {
+    const DevRun rn = a.runs[run];
+    one_shard = a.shard_ptrs[rn.slot] + ((int64_t)m.src_row - rn.row0) * (int64_t)m.cols +
+                (int64_t)m.bj * kTile;
+  }
+  for (int rb = wg; rb < kTile; rb += kGroupWarps * kRowsAtOnce) {
+    uint16_t e[kRowsAtOnce][kTile / 32];
+#pragma unroll
+    for (int i = 0; i < kRowsAtOnce; ++i) {
+      const int r = rb + i * kGroupWarps;
+      const uint16_t* row = r < nrows ? gather_row(a, m, run, one_shard, r) : nullptr;
+#pragma unroll
+      for (int c4 = 0; c4 < kTile / 32; ++c4) {
+        const int c = lane + 32 * c4;
+        e[i][c4] = (row && c < ncols) ? ld_nc_u16(row + c) : (uint16_t)0;
+      }
     }
-    uint16_t* out = reinterpret_cast<uint16_t*>(sp + r * kRowBytes);
-    for (int c = lane; c < kTile; c += 32) out[c] = (row && c < ncols) ? ld_nc_u16(row + c) : (uint16_t)0;
+#pragma unroll
+    for (int i = 0; i < kRowsAtOnce; ++i) {
+      uint16_t* out = reinterpret_cast<uint16_t*>(sp + (rb + i * kGroupWarps) * kRowBytes);
+#pragma unroll
+      for (int c4 = 0; c4 < kTile / 32; ++c4) out[lane + 32 * c4] = e[i][c4];
+    }
   }
 }
 
