@@ -38,11 +38,17 @@ class _Param(C.Structure):
                 ("shard_rows", C.POINTER(C.c_int64))]
 
 
+class _Slice(C.Structure):
+    _fields_ = [("dim", C.c_int32), ("num_ranges", C.c_int32),
+                ("begin", C.POINTER(C.c_int64)), ("length", C.POINTER(C.c_int64))]
+
+
 class _Output(C.Structure):
     _fields_ = [("num_parts", C.c_int32), ("parts", C.POINTER(C.c_int32)),
                 ("fp8", C.c_int32), ("num_dsts", C.c_int32),
                 ("dst_rank", C.POINTER(C.c_int32)),
-                ("data_off", C.POINTER(C.c_uint64)), ("scale_off", C.POINTER(C.c_uint64))]
+                ("data_off", C.POINTER(C.c_uint64)), ("scale_off", C.POINTER(C.c_uint64)),
+                ("dst_slice", C.POINTER(_Slice))]
 
 
 class _Model(C.Structure):
@@ -72,6 +78,8 @@ def lib():
         L.wo_quantize_element.argtypes = [C.c_uint16, C.c_float]
         L.wo_output_shape.argtypes = [C.POINTER(_Model), C.c_int32, C.POINTER(C.c_int64),
                                       C.POINTER(C.c_int64)]
+        L.wo_dst_shape.argtypes = [C.POINTER(_Model), C.c_int32, C.c_int32,
+                                   C.POINTER(C.c_int64), C.POINTER(C.c_int64)]
         L.wo_layout.argtypes = [C.POINTER(_Model), C.c_void_p, C.c_void_p, C.c_void_p]
         L.wo_prepare_output.argtypes = [C.POINTER(_Model), C.c_int32, C.c_void_p, C.c_void_p,
                                         C.c_void_p]
@@ -139,11 +147,31 @@ class Model:
                 soff = (C.c_uint64 * len(o.dst_ranks))(
                     *[OFFSET_AUTO if v is None else v for v in o.scale_off])
                 self._keep.append(soff)
+            slices = None
+            if getattr(o, "slices", None) is not None:
+                slices = (_Slice * len(o.dst_ranks))()
+                for d, sl in enumerate(o.slices):
+                    if sl is None:
+                        slices[d] = _Slice(0, 0, None, None)
+                        continue
+                    dim, ranges = sl
+                    b = (C.c_int64 * len(ranges))(*[r[0] for r in ranges])
+                    n = (C.c_int64 * len(ranges))(*[r[1] for r in ranges])
+                    self._keep += [b, n]
+                    slices[d] = _Slice(dim, len(ranges), b, n)
+                self._keep.append(slices)
             outs[i] = _Output(len(o.parts), parts, int(bool(o.fp8)), len(o.dst_ranks), ranks,
-                              doff, soff)
+                              doff, soff, slices)
         self._params, self._outs = params, outs
         self.c = _Model(len(w.params), params, len(w.outputs), outs, w.num_ranks)
         self.num_dsts = sum(len(o.dst_ranks) for o in w.outputs)
+
+    def dst_shape(self, o: int, d: int) -> tuple:
+        """(rows, cols) that destination d of output o holds."""
+        r, c = C.c_int64(), C.c_int64()
+        if lib().wo_dst_shape(C.byref(self.c), o, d, C.byref(r), C.byref(c)):
+            raise ValueError("oracle: invalid slice")
+        return r.value, c.value
 
     def layout(self):
         """(data_off, scale_off) as lists per output of per-destination

@@ -161,6 +161,40 @@ static uint64_t scale_bytes(const wo_output* out, int64_t r, int64_t c) {
   return out->fp8 ? (uint64_t)(ceil_div(r, TILE) * ceil_div(c, TILE)) * 4u : 0u;
 }
 
+/* The slice of destination d, or NULL for the whole tensor. */
+static const wo_slice* dst_slice(const wo_output* out, int32_t d) {
+  if (!out->dst_slice || out->dst_slice[d].num_ranges == 0) return NULL;
+  return &out->dst_slice[d];
+}
+
+/* READING (tensor-parallel destinations): a destination may take 128-aligned
+ * row ranges (column-parallel layers) or column ranges (row-parallel layers)
+ * of the fused tensor; it holds their concatenation. */
+int wo_dst_shape(const wo_model* m, int32_t o, int32_t d, int64_t* rows, int64_t* cols) {
+  int64_t r, c;
+  if (wo_output_shape(m, o, &r, &c)) return -1;
+  const wo_slice* sl = dst_slice(&m->outputs[o], d);
+  if (!sl) {
+    *rows = r;
+    *cols = c;
+    return 0;
+  }
+  if (sl->dim != 0 && sl->dim != 1) return -1;
+  const int64_t extent = sl->dim == 0 ? r : c;
+  int64_t total = 0;
+  for (int32_t k = 0; k < sl->num_ranges; ++k) {
+    const int64_t b = sl->begin[k], n = sl->length[k];
+    if (b < 0 || n < 1 || b % TILE || b + n > extent) return -1;
+    if (n % TILE && !(b + n == extent && k == sl->num_ranges - 1)) return -1;
+    for (int32_t q = 0; q < k; ++q)   /* no overlap with an earlier range */
+      if (b < sl->begin[q] + sl->length[q] && sl->begin[q] < b + n) return -1;
+    total += n;
+  }
+  *rows = sl->dim == 0 ? total : r;
+  *cols = sl->dim == 0 ? c : total;
+  return 0;
+}
+
 int wo_layout(const wo_model* m, uint64_t* data_off, uint64_t* scale_off,
               uint64_t* pool_bytes) {
   for (int32_t rank = 0; rank < m->num_ranks; ++rank) {
@@ -168,9 +202,9 @@ int wo_layout(const wo_model* m, uint64_t* data_off, uint64_t* scale_off,
     uint64_t explicit_end = 0;
     for (int32_t o = 0; o < m->num_outputs; ++o) {
       const wo_output* out = &m->outputs[o];
-      int64_t r, c;
-      if (wo_output_shape(m, o, &r, &c)) return -1;
       for (int32_t d = 0; d < out->num_dsts; ++d) {
+        int64_t r, c;
+        if (wo_dst_shape(m, o, d, &r, &c)) return -1;
         if (out->dst_rank[d] != rank) continue;
         if (out->data_off && out->data_off[d] != WO_OFFSET_AUTO) {
           uint64_t e = out->data_off[d] + data_bytes(out, r, c);
@@ -188,10 +222,10 @@ int wo_layout(const wo_model* m, uint64_t* data_off, uint64_t* scale_off,
     int64_t flat = 0;
     for (int32_t o = 0; o < m->num_outputs; ++o) {
       const wo_output* out = &m->outputs[o];
-      int64_t r, c;
-      wo_output_shape(m, o, &r, &c);
       for (int32_t d = 0; d < out->num_dsts; ++d, ++flat) {
         if (out->dst_rank[d] != rank) continue;
+        int64_t r, c;
+        wo_dst_shape(m, o, d, &r, &c);
         uint64_t doff, soff = 0;
         if (out->data_off && out->data_off[d] != WO_OFFSET_AUTO) {
           doff = out->data_off[d];
@@ -289,6 +323,55 @@ int wo_prepare_output(const wo_model* m, int32_t o,
   return 0;
 }
 
+/* Copy the slice sl of a prepared output (data: rows x cols elements of
+ * esize bytes; scales: its block grid) into a destination: the ranges'
+ * rows or columns, concatenated in order, and the same ranges of block
+ * rows or block columns of the grid. */
+static void copy_slice(const wo_output* out, const wo_slice* sl, int64_t rows, int64_t cols,
+                       const uint8_t* data, const float* scales, uint8_t* dst_data,
+                       float* dst_scales) {
+  const int64_t es = out->fp8 ? 1 : 2;
+  const int64_t tiles_n = ceil_div(cols, TILE), tiles_m = ceil_div(rows, TILE);
+  if (sl->dim == 0) {
+    int64_t at = 0, sat = 0;
+    for (int32_t k = 0; k < sl->num_ranges; ++k) {
+      const int64_t b = sl->begin[k], n = sl->length[k];
+      memcpy(dst_data + at * cols * es, data + b * cols * es, (size_t)(n * cols * es));
+      at += n;
+      if (dst_scales) {
+        const int64_t nb = ceil_div(n, TILE);
+        memcpy(dst_scales + sat * tiles_n, scales + (b / TILE) * tiles_n,
+               (size_t)(nb * tiles_n) * sizeof(float));
+        sat += nb;
+      }
+    }
+  } else {
+    int64_t width = 0, swidth = 0;
+    for (int32_t k = 0; k < sl->num_ranges; ++k) {
+      width += sl->length[k];
+      swidth += ceil_div(sl->length[k], TILE);
+    }
+    for (int64_t r = 0; r < rows; ++r) {
+      int64_t at = 0;
+      for (int32_t k = 0; k < sl->num_ranges; ++k) {
+        const int64_t b = sl->begin[k], n = sl->length[k];
+        memcpy(dst_data + (r * width + at) * es, data + (r * cols + b) * es, (size_t)(n * es));
+        at += n;
+      }
+    }
+    if (dst_scales)
+      for (int64_t bi = 0; bi < tiles_m; ++bi) {
+        int64_t at = 0;
+        for (int32_t k = 0; k < sl->num_ranges; ++k) {
+          const int64_t nb = ceil_div(sl->length[k], TILE);
+          memcpy(dst_scales + bi * swidth + at, scales + bi * tiles_n + sl->begin[k] / TILE,
+                 (size_t)nb * sizeof(float));
+          at += nb;
+        }
+      }
+  }
+}
+
 typedef struct {
   const wo_model* m;
   const uint64_t* data_off;
@@ -318,8 +401,14 @@ static void* worker(void* argp) {
     for (int32_t q = 0; q < o; ++q) flat += m->outputs[q].num_dsts;
     for (int32_t d = 0; d < out->num_dsts; ++d) {
       uint8_t* pool = a->pools[out->dst_rank[d]];
-      memcpy(pool + a->data_off[flat + d], data, db);
-      if (out->fp8) memcpy(pool + a->scale_off[flat + d], scales, sb);
+      const wo_slice* sl = dst_slice(out, d);
+      if (!sl) {
+        memcpy(pool + a->data_off[flat + d], data, db);
+        if (out->fp8) memcpy(pool + a->scale_off[flat + d], scales, sb);
+      } else {
+        copy_slice(out, sl, rows, cols, data, scales, pool + a->data_off[flat + d],
+                   out->fp8 ? (float*)(pool + a->scale_off[flat + d]) : NULL);
+      }
     }
     free(data);
     free(scales);

@@ -22,7 +22,8 @@
  *       over the whole non-saturating fp32 range.
  *   wo_tile_scale, wo_quantize_element : numpy float32 division, the
  *       dequantisation error bound, exact-rational brute force.
- *   wo_layout : closed-form pool sizes, disjointness, explicit offsets.
+ *   wo_layout, wo_dst_shape : closed-form pool sizes, disjointness, explicit
+ *       offsets; slices against numpy slicing of the whole output.
  *   wo_prepare_output / wo_prepare : torch.cat of the shards (reassembly and
  *       fusion), numpy amax, exact-rational brute force on tiny tensors.
  */
@@ -44,10 +45,25 @@ typedef struct {
   const int64_t* shard_rows;
 } wo_param;
 
+/* The part of an output one destination takes: the listed row ranges
+ * (dim 0) or column ranges (dim 1) of the fused tensor, concatenated in
+ * order, with the matching block rows / columns of the scale grid.
+ * num_ranges == 0 means the whole tensor. Each range starts at a multiple
+ * of 128 and is a multiple of 128 long, except that the last range may end
+ * at the tensor's edge; ranges do not overlap. */
+typedef struct {
+  int32_t dim;
+  int32_t num_ranges;
+  const int64_t* begin;
+  const int64_t* length;
+} wo_slice;
+
 /* One output tensor: the row concatenation of its parts, written as BF16
  * bytes (fp8 == 0) or as e4m3 codes plus a 128x128 fp32 scale grid
  * (fp8 == 1), once per destination. data_off / scale_off may be NULL or
- * hold WO_OFFSET_AUTO entries, which the layout packs. */
+ * hold WO_OFFSET_AUTO entries, which the layout packs. dst_slice may be
+ * NULL (every destination takes the whole tensor) or hold one slice per
+ * destination. */
 typedef struct {
   int32_t num_parts;
   const int32_t* parts;
@@ -56,6 +72,7 @@ typedef struct {
   const int32_t* dst_rank;
   const uint64_t* data_off;
   const uint64_t* scale_off;
+  const wo_slice* dst_slice;
 } wo_output;
 
 typedef struct {
@@ -84,6 +101,10 @@ uint8_t wo_quantize_element(uint16_t x_bits, float s);
 
 /* Output shape after fusion. Returns 0, or -1 if the parts disagree. */
 int wo_output_shape(const wo_model* m, int32_t o, int64_t* rows, int64_t* cols);
+
+/* Shape of what destination d of output o holds (its slice, or the whole
+ * tensor). Returns 0, or -1 if the slice breaks the rules above. */
+int wo_dst_shape(const wo_model* m, int32_t o, int32_t d, int64_t* rows, int64_t* cols);
 
 /* Destination offsets (flat over outputs, then destinations) and pool sizes.
  * Returns 0 or -1 on an invalid model. */

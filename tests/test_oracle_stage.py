@@ -247,3 +247,101 @@ def test_prepare_covers_every_scheduled_byte_once(oracle_mod):
                 mask[off:off + n] = True
         assert np.array_equal(a[rank][mask], b[rank][mask])
         assert np.all(a[rank][~mask] == 0x00) and np.all(b[rank][~mask] == 0xFF)
+
+
+# --------------------------------------------------------------------------
+# tensor-parallel destination slices
+# --------------------------------------------------------------------------
+
+def _sliced_workload():
+    """An FP8 output fused from two parts (300 x 260: partial blocks in both
+    dimensions) and a BF16 output, each sent whole and as row / column
+    slices, in and out of order, including ranges that end at the edge."""
+    params = [Param("a1", 172, 260, (100, 72)), Param("a2", 128, 260, (128,)),
+              Param("b", 200, 136, (64, 136))]
+    fp8_slices = (None, (0, ((128, 128), (0, 128))), (0, ((256, 44),)),
+                  (1, ((128, 132),)), (1, ((0, 128), (256, 4))))
+    bf16_slices = (None, (0, ((0, 128), (128, 72))), (1, ((128, 8),)))
+    outs = [Output("a", (0, 1), True, (0, 1, 0, 1, 0), slices=fp8_slices),
+            Output("b", (2,), False, (1, 0, 1), slices=bf16_slices)]
+    return Workload("sliced", params, outs, 2, ValueRecipe("student_t3", 0.02, 41))
+
+
+def _expected_slice(data, scales, shape, sl, fp8):
+    """numpy slicing of a whole prepared output (codes and block scales)."""
+    m, n = shape
+    es = 1 if fp8 else 2
+    arr = data.reshape(m, n * es)
+    grid = scales.reshape(-(-m // 128), -(-n // 128)) if fp8 else None
+    if sl is None:
+        return arr.ravel(), (grid.ravel() if fp8 else None)
+    dim, ranges = sl
+    if dim == 0:
+        d = np.concatenate([arr[b:b + k] for b, k in ranges])
+        g = np.concatenate([grid[b // 128:-(-(b + k) // 128)] for b, k in ranges]) if fp8 else None
+    else:
+        d = np.concatenate([arr[:, b * es:(b + k) * es] for b, k in ranges], axis=1)
+        g = (np.concatenate([grid[:, b // 128:-(-(b + k) // 128)] for b, k in ranges], axis=1)
+             if fp8 else None)
+    return d.ravel(), (g.ravel() if fp8 else None)
+
+
+def test_slices_equal_numpy_slicing_of_the_whole_output(oracle_mod):
+    w = _sliced_workload()
+    flat = shards_to_host_u16(make_shards(w))
+    m = oracle_mod.Model(w)
+    pools = m.prepare(flat, nthreads=2)
+    d_off, s_off, _ = m.layout()
+    for o, out in enumerate(w.outputs):
+        data, scales = m.prepare_output(o, flat)
+        for d, rank in enumerate(out.dst_ranks):
+            sl = out.slices[d]
+            want_d, want_s = _expected_slice(data, scales, w.output_shape(o), sl, out.fp8)
+            assert m.dst_shape(o, d) == w.dst_shape(o, d)
+            got_d = pools[rank][d_off[o][d]:d_off[o][d] + want_d.size]
+            assert np.array_equal(got_d, want_d), (out.name, d)
+            if out.fp8:
+                got_s = pools[rank][s_off[o][d]:s_off[o][d] + 4 * want_s.size].view(np.float32)
+                assert np.array_equal(got_s.view(np.uint32), want_s.view(np.uint32)), (out.name, d)
+
+
+def test_tensor_parallel_slices_reassemble_the_tensor(oracle_mod):
+    """Row slices that partition the fused tensor, concatenated in range
+    order, are the whole output; so are column slices side by side."""
+    params = [Param("g", 512, 384, (128,) * 4), Param("u", 512, 384, (256, 256)),
+              Param("g2", 512, 384, (512,)), Param("u2", 512, 384, (512,))]
+    tp = 2
+    rows = [(0, ((r * 256, 256), (512 + r * 256, 256))) for r in range(tp)]   # gate_r, up_r
+    cols = [(1, ((c * 128, 128),)) for c in range(3)]
+    outs = [Output("gu", (0, 1), True, tuple(range(tp)), slices=tuple(rows)),
+            Output("gu_cols", (2, 3), True, (0, 1, 0), slices=tuple(cols))]
+    w = Workload("tp", params, outs, tp, ValueRecipe("normal", 0.02, 43))
+    flat = shards_to_host_u16(make_shards(w))
+    m = oracle_mod.Model(w)
+    pools = m.prepare(flat, nthreads=2)
+    d_off, s_off, _ = m.layout()
+    data, scales = m.prepare_output(0, flat)
+    whole = data.reshape(1024, 384)
+    grid = scales.reshape(8, 3)
+    pieces, gpieces = {}, {}
+    for r in range(tp):
+        blob = pools[r][d_off[0][r]:d_off[0][r] + 512 * 384].reshape(512, 384)
+        sb = pools[r][s_off[0][r]:s_off[0][r] + 4 * 4 * 3].view(np.float32).reshape(4, 3)
+        pieces[r * 256], pieces[512 + r * 256] = blob[:256], blob[256:]
+        gpieces[r * 2], gpieces[4 + r * 2] = sb[:2], sb[2:]
+    assert np.array_equal(np.concatenate([pieces[k] for k in sorted(pieces)]), whole)
+    assert np.array_equal(np.concatenate([gpieces[k] for k in sorted(gpieces)]).view(np.uint32),
+                          grid.view(np.uint32))
+    data2, scales2 = m.prepare_output(1, flat)
+    cols_got = [pools[out_rank][d_off[1][d]:d_off[1][d] + 1024 * 128].reshape(1024, 128)
+                for d, out_rank in enumerate(outs[1].dst_ranks)]
+    assert np.array_equal(np.concatenate(cols_got, axis=1), data2.reshape(1024, 384))
+
+
+@pytest.mark.parametrize("sl", [(0, ((64, 128),)), (0, ((0, 100), (128, 128))), (0, ((0, 256), (128, 128))),
+                                (0, ((256, 128),)), (1, ((0, 200),)), (2, ((0, 128),)), (0, ((0, 0),))])
+def test_invalid_slices_are_rejected(oracle_mod, sl):
+    w = Workload("bad", [Param("p", 300, 260, (300,))],
+                 [Output("p", (0,), True, (0,), slices=(sl,))], 1)
+    with pytest.raises(ValueError):
+        oracle_mod.Model(w).layout()

@@ -57,6 +57,9 @@ class Output:
     dst_ranks: tuple
     data_off: Optional[tuple] = None    # None or per-destination offset / None=auto
     scale_off: Optional[tuple] = None
+    # None, or per destination: None (whole tensor) or (dim, ((begin, length), ...)),
+    # the row (dim 0) or column (dim 1) ranges that destination takes
+    slices: Optional[tuple] = None
 
 
 @dataclass(frozen=True)
@@ -86,6 +89,16 @@ class Workload:
             raise ValueError(f"fusion parts of {out.name} differ in cols")
         return sum(self.params[p].rows for p in out.parts), cols.pop()
 
+    def dst_shape(self, o: int, d: int) -> tuple:
+        """(rows, cols) that destination d of output o holds."""
+        m, n = self.output_shape(o)
+        out = self.outputs[o]
+        if out.slices is None or out.slices[d] is None:
+            return m, n
+        dim, ranges = out.slices[d]
+        total = sum(r[1] for r in ranges)
+        return (total, n) if dim == 0 else (m, total)
+
     @property
     def num_params_total(self) -> int:
         return sum(p.numel for p in self.params)
@@ -100,11 +113,11 @@ class Workload:
         """Destination bytes written by one pass (data + scales, all dsts)."""
         total = 0
         for o, out in enumerate(self.outputs):
-            m, n = self.output_shape(o)
-            per = m * n if out.fp8 else 2 * m * n
-            if out.fp8:
-                per += 4 * (-(-m // TILE)) * (-(-n // TILE))
-            total += per * len(out.dst_ranks)
+            for d in range(len(out.dst_ranks)):
+                m, n = self.dst_shape(o, d)
+                total += m * n if out.fp8 else 2 * m * n
+                if out.fp8:
+                    total += 4 * (-(-m // TILE)) * (-(-n // TILE))
         return total
 
     @property
@@ -128,7 +141,7 @@ class Workload:
         for o in outputs:
             out = self.outputs[o]
             outs.append(Output(out.name, tuple(remap[p] for p in out.parts), out.fp8,
-                               out.dst_ranks, out.data_off, out.scale_off))
+                               out.dst_ranks, out.data_off, out.scale_off, out.slices))
         return Workload(name or f"{self.name}[subset]", [self.params[p] for p in keep_params],
                         outs, self.num_ranks, self.values)
 
