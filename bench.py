@@ -4,7 +4,8 @@ experts + 1 shared, w1/w3 2048x7168 fused to gate_up 4096x7168, w2
 ranks; 16.96 G params, 33.9 GB BF16 read, 16.96 GB written per step).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
-                  [--workload kimi_k2_moe_layer|offload_8layer] [--images K]
+                  [--workload kimi_k2_moe_layer|llama_dense|llama_dense_tp4|edge_stress|
+                              tiny_dense|offload_8layer] [--images K]
                   [--no-e2e] [--no-cpu-baseline] [--experts E]
 
 Prints one JSON line. `value` is GB/s of BF16 input for the whole job
@@ -226,8 +227,8 @@ def main():
     ap.add_argument("--cpu-experts", type=int, default=8)
     ap.add_argument("--reference-experts", type=int, default=2)
     ap.add_argument("--workload", default="kimi_k2_moe_layer",
-                    choices=["kimi_k2_moe_layer", "llama_dense", "edge_stress", "tiny_dense",
-                             "offload_8layer"])
+                    choices=["kimi_k2_moe_layer", "llama_dense", "llama_dense_tp4", "edge_stress",
+                             "tiny_dense", "offload_8layer"])
     ap.add_argument("--images", type=int, default=2)
     ap.add_argument("--stack-steps", type=int, default=2)
     ap.add_argument("--stack-warmup", type=int, default=1)

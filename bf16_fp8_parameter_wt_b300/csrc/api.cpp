@@ -92,6 +92,8 @@ wt_status upload(Plan& p, int device) {
   const size_t o_dyn = take(dl.bytes);
   const size_t o_units = take(p.h_units.size() * sizeof(DevUnit));
   const size_t o_runs = take(p.h_runs.size() * sizeof(DevRun));
+  const size_t o_geom = take(p.h_geom.size() * sizeof(DevDstGeom));
+  const size_t o_bmap = take(p.h_blockmap.size() * sizeof(int32_t));
   const size_t o_err = take(sizeof(int32_t));
   const size_t o_offl_s = take(offload ? n_slots * sizeof(void*) : 0);
   const size_t o_offl_t = take(offload ? n_slots * kTmapBytes : 0);
@@ -104,6 +106,8 @@ wt_status upload(Plan& p, int device) {
   if ((e = cudaMemset(base + o_dyn, 0, dl.bytes)) != cudaSuccess ||
       (e = put(o_units, p.h_units.data(), p.h_units.size() * sizeof(DevUnit))) != cudaSuccess ||
       (e = put(o_runs, p.h_runs.data(), p.h_runs.size() * sizeof(DevRun))) != cudaSuccess ||
+      (e = put(o_geom, p.h_geom.data(), p.h_geom.size() * sizeof(DevDstGeom))) != cudaSuccess ||
+      (e = put(o_bmap, p.h_blockmap.data(), p.h_blockmap.size() * sizeof(int32_t))) != cudaSuccess ||
       (e = cudaMemset(base + o_err, 0, sizeof(int32_t))) != cudaSuccess)
     return cuda_fail(e, "uploading plan tables");
   p.dyn_bytes = dl.bytes;
@@ -114,6 +118,8 @@ wt_status upload(Plan& p, int device) {
   p.args.units = reinterpret_cast<const DevUnit*>(base + o_units);
   p.args.runs = reinterpret_cast<const DevRun*>(base + o_runs);
   p.args.dst_ptrs = p.d_dst_ptrs;
+  p.args.geom = reinterpret_cast<const DevDstGeom*>(base + o_geom);
+  p.args.blockmap = reinterpret_cast<const int32_t*>(base + o_bmap);
   p.args.error_word = p.d_error;
   p.args.timeout_ns = kDefaultTimeoutNs;
 

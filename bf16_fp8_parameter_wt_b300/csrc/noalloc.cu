@@ -75,14 +75,16 @@ extern "C" wt_status wt_prepare_noalloc(const wt_plan_desc* desc, const void* co
   if (st != WT_OK) return st;
 
   // table image: shard pointers, their tensor maps, destinations, unit
-  // descriptors, row runs, error word
+  // descriptors, row runs, destination geometry and block maps, error word
   const size_t n_slots = (size_t)p.num_slots;
   const size_t o_shards = 0;
   const size_t o_tmaps = up256(o_shards + n_slots * sizeof(void*));
   const size_t o_dsts = up256(o_tmaps + n_slots * kTmapBytes);
   const size_t o_units = up256(o_dsts + (size_t)p.num_dst_entries * sizeof(DevDstPtr));
   const size_t o_runs = up256(o_units + p.h_units.size() * sizeof(DevUnit));
-  const size_t o_err = up256(o_runs + p.h_runs.size() * sizeof(DevRun));
+  const size_t o_geom = up256(o_runs + p.h_runs.size() * sizeof(DevRun));
+  const size_t o_bmap = up256(o_geom + p.h_geom.size() * sizeof(DevDstGeom));
+  const size_t o_err = up256(o_bmap + p.h_blockmap.size() * sizeof(int32_t));
   const size_t total = o_err + 256;
   if (total > kNoAllocScratchBytes)
     return fail_na(WT_ERR_INVALID_ARGUMENT,
@@ -134,6 +136,9 @@ extern "C" wt_status wt_prepare_noalloc(const wt_plan_desc* desc, const void* co
     }
   if (!p.h_units.empty()) std::memcpy(h + o_units, p.h_units.data(), p.h_units.size() * sizeof(DevUnit));
   if (!p.h_runs.empty()) std::memcpy(h + o_runs, p.h_runs.data(), p.h_runs.size() * sizeof(DevRun));
+  if (!p.h_geom.empty()) std::memcpy(h + o_geom, p.h_geom.data(), p.h_geom.size() * sizeof(DevDstGeom));
+  if (!p.h_blockmap.empty())
+    std::memcpy(h + o_bmap, p.h_blockmap.data(), p.h_blockmap.size() * sizeof(int32_t));
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   // from pageable memory: the call returns once the image has been staged
@@ -149,6 +154,8 @@ extern "C" wt_status wt_prepare_noalloc(const wt_plan_desc* desc, const void* co
   a.runs = reinterpret_cast<const DevRun*>(dbase + o_runs);
   a.shard_ptrs = reinterpret_cast<const uint16_t* const*>(dbase + o_shards);
   a.dst_ptrs = reinterpret_cast<const DevDstPtr*>(dbase + o_dsts);
+  a.geom = reinterpret_cast<const DevDstGeom*>(dbase + o_geom);
+  a.blockmap = reinterpret_cast<const int32_t*>(dbase + o_bmap);
   a.unit_begin = 0;
   a.unit_end = p.num_units;
   a.error_word = reinterpret_cast<int32_t*>(dbase + o_err);

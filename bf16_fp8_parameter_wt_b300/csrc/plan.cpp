@@ -35,6 +35,44 @@ struct Range {
   bool scale;
 };
 
+// Destination k of output oi: the slice it takes (if any) and its sizes.
+// A slice is the listed 128-aligned row (dim 0) or column (dim 1) ranges
+// of the fused tensor, concatenated; only the last range may end off the
+// 128 grid, at the tensor's edge; ranges do not overlap.
+wt_status parse_slice(const wt_slice_desc* sd, OutputInfo& oi, int k) {
+  DstInfo& ds = oi.dsts[k];
+  const std::string where = oi.name + ", destination " + std::to_string(k) + ": ";
+  ds.rows = oi.rows;
+  ds.cols = oi.cols;
+  if (sd && sd->num_ranges != 0) {
+    if (sd->num_ranges < 0 || !sd->begin || !sd->length)
+      return fail(WT_ERR_INVALID_ARGUMENT, where + "slice ranges missing");
+    if (sd->dim != 0 && sd->dim != 1) return fail(WT_ERR_INVALID_ARGUMENT, where + "slice dim must be 0 or 1");
+    const int64_t extent = sd->dim == 0 ? oi.rows : oi.cols;
+    int64_t total = 0;
+    for (int32_t r = 0; r < sd->num_ranges; ++r) {
+      const int64_t b = sd->begin[r], n = sd->length[r];
+      if (b < 0 || n < 1 || b + n > extent)
+        return fail(WT_ERR_SHAPE, where + "slice range " + std::to_string(r) + " is outside the tensor");
+      if (b % kTile) return fail(WT_ERR_SHAPE, where + "slice range does not start on a multiple of 128");
+      if (n % kTile && !(b + n == extent && r == sd->num_ranges - 1))
+        return fail(WT_ERR_SHAPE, where + "only the last slice range may end off the 128 grid, at the edge");
+      for (int32_t q = 0; q < r; ++q)
+        if (b < sd->begin[q] + sd->length[q] && sd->begin[q] < b + n)
+          return fail(WT_ERR_SHAPE, where + "slice ranges overlap");
+      total += n;
+    }
+    ds.slice_dim = sd->dim;
+    ds.slice_begin.assign(sd->begin, sd->begin + sd->num_ranges);
+    ds.slice_len.assign(sd->length, sd->length + sd->num_ranges);
+    if (sd->dim == 0) ds.rows = total; else ds.cols = total;
+  }
+  const bool fp8 = oi.format == WT_OUT_FP8_E4M3_B128;
+  ds.data_bytes = uint64_t(ds.rows * ds.cols) * (fp8 ? 1u : 2u);
+  ds.scale_bytes = fp8 ? uint64_t(ceil_div(ds.rows, kTile) * ceil_div(ds.cols, kTile)) * 4u : 0u;
+  return WT_OK;
+}
+
 }  // namespace
 
 wt_status compile_plan(const wt_plan_desc* d, Plan* p) {
@@ -139,8 +177,10 @@ wt_status compile_plan(const wt_plan_desc* d, Plan* p) {
         return fail(WT_ERR_INVALID_ARGUMENT, oi.name + ": explicit offset out of range");
       oi.dsts[k].data_off = doff;
       oi.dsts[k].scale_off = soff;
+      wt_status st = parse_slice(od.dst_slices ? &od.dst_slices[k] : nullptr, oi, k);
+      if (st != WT_OK) return st;
+      p->bytes_written += oi.dsts[k].data_bytes + oi.dsts[k].scale_bytes;
     }
-    p->bytes_written += (oi.data_bytes + oi.scale_bytes) * (uint64_t)od.num_dsts;
     p->bytes_read += uint64_t(rows * cols) * 2u;
   }
   for (int i = 0; i < d->num_params; ++i)
@@ -156,21 +196,21 @@ wt_status compile_plan(const wt_plan_desc* d, Plan* p) {
   for (auto& oi : p->outputs)
     for (auto& ds : oi.dsts) {
       if (ds.data_off != WT_OFFSET_AUTO)
-        cursor[ds.rank] = std::max(cursor[ds.rank], ds.data_off + oi.data_bytes);
+        cursor[ds.rank] = std::max(cursor[ds.rank], ds.data_off + ds.data_bytes);
       if (oi.format == WT_OUT_FP8_E4M3_B128 && ds.scale_off != WT_OFFSET_AUTO)
-        cursor[ds.rank] = std::max(cursor[ds.rank], ds.scale_off + oi.scale_bytes);
+        cursor[ds.rank] = std::max(cursor[ds.rank], ds.scale_off + ds.scale_bytes);
     }
   for (auto& oi : p->outputs)
     for (auto& ds : oi.dsts) {
       uint64_t& c = cursor[ds.rank];
       if (ds.data_off == WT_OFFSET_AUTO) {
         ds.data_off = align_up(c, 256);
-        c = ds.data_off + oi.data_bytes;
+        c = ds.data_off + ds.data_bytes;
       }
       if (oi.format == WT_OUT_FP8_E4M3_B128) {
         if (ds.scale_off == WT_OFFSET_AUTO) {
           ds.scale_off = align_up(c, 256);
-          c = ds.scale_off + oi.scale_bytes;
+          c = ds.scale_off + ds.scale_bytes;
         }
       } else {
         ds.scale_off = 0;
@@ -182,9 +222,9 @@ wt_status compile_plan(const wt_plan_desc* d, Plan* p) {
     auto& oi = p->outputs[o];
     for (int k = 0; k < (int)oi.dsts.size(); ++k) {
       auto& ds = oi.dsts[k];
-      per_rank[ds.rank].push_back({ds.data_off, oi.data_bytes, o, k, false});
+      per_rank[ds.rank].push_back({ds.data_off, ds.data_bytes, o, k, false});
       if (oi.format == WT_OUT_FP8_E4M3_B128)
-        per_rank[ds.rank].push_back({ds.scale_off, oi.scale_bytes, o, k, true});
+        per_rank[ds.rank].push_back({ds.scale_off, ds.scale_bytes, o, k, true});
     }
   }
   for (int r = 0; r < d->num_ranks; ++r) {
@@ -208,6 +248,8 @@ wt_status compile_plan(const wt_plan_desc* d, Plan* p) {
   // ---- device tables: units, row runs, per-slot shapes -------------------
   p->h_units.clear();
   p->h_runs.clear();
+  p->h_geom.clear();
+  p->h_blockmap.clear();
   p->h_units.reserve((size_t)units);
   p->slot_rows.assign(p->num_slots, 0);
   p->slot_cols.assign(p->num_slots, 0);
@@ -223,6 +265,27 @@ wt_status compile_plan(const wt_plan_desc* d, Plan* p) {
     auto& oi = p->outputs[o];
     oi.dst_begin = dst_entries;
     dst_entries += (int32_t)oi.dsts.size();
+    // where each block lands in each destination
+    const int64_t tiles_m = ceil_div(oi.rows, kTile), tiles_n_all = ceil_div(oi.cols, kTile);
+    bool sliced = false;
+    for (const DstInfo& ds : oi.dsts) {
+      DevDstGeom g;
+      g.dim = ds.slice_dim;
+      g.map_off = -1;
+      g.ld = (uint32_t)ds.cols;
+      g.sld = (uint32_t)ceil_div(ds.cols, kTile);
+      if (ds.slice_dim >= 0) {
+        sliced = true;
+        g.map_off = (int32_t)p->h_blockmap.size();
+        const int64_t nblk = ds.slice_dim == 0 ? tiles_m : tiles_n_all;
+        p->h_blockmap.resize(p->h_blockmap.size() + (size_t)nblk, -1);
+        int32_t at = 0;
+        for (size_t r = 0; r < ds.slice_begin.size(); ++r)
+          for (int64_t b = ds.slice_begin[r] / kTile; b < ceil_div(ds.slice_begin[r] + ds.slice_len[r], kTile); ++b)
+            p->h_blockmap[(size_t)g.map_off + (size_t)b] = at++;
+      }
+      p->h_geom.push_back(g);
+    }
     // the runs of this output: shards of its parts in fusion order, empty
     // shards skipped (reassembly: row r of the part comes from the shard
     // whose row range holds r)
@@ -248,7 +311,7 @@ wt_status compile_plan(const wt_plan_desc* d, Plan* p) {
       const bool single = run.row0 + run.rows >= r0 + nrows;
       // one shard and 16-byte rows: one 2-D tensor copy from that shard
       const bool tma = single && oi.vec;
-      const uint32_t f = flags | (single ? 0u : kUnitMulti);
+      const uint32_t f = flags | (single ? 0u : kUnitMulti) | (sliced ? kUnitSliced : 0u);
       for (int64_t bj = 0; bj < tiles_n; ++bj) {
         const int64_t ncols = std::min<int64_t>(kTile, oi.cols - bj * kTile);
         DevUnit u;
@@ -260,6 +323,23 @@ wt_status compile_plan(const wt_plan_desc* d, Plan* p) {
         u.shape = (uint32_t)(nrows - 1) | ((uint32_t)(ncols - 1) << 8) | (f << 16);
         u.num_dsts = (uint32_t)oi.dsts.size();
         u.dst_begin = (uint32_t)oi.dst_begin;
+        if (sliced) {
+          // the destinations that hold this block: when exactly one does,
+          // the unit names it alone (the kernel's single-destination path)
+          int32_t held = 0, which = -1;
+          for (size_t k = 0; k < oi.dsts.size(); ++k) {
+            const DevDstGeom& g = p->h_geom[(size_t)oi.dst_begin + k];
+            const bool in = g.dim < 0 || p->h_blockmap[(size_t)g.map_off + (size_t)(g.dim == 0 ? bi : bj)] >= 0;
+            if (in) {
+              ++held;
+              which = (int32_t)k;
+            }
+          }
+          if (held <= 1) {
+            u.num_dsts = (uint32_t)held;
+            u.dst_begin = (uint32_t)(oi.dst_begin + std::max(which, 0));
+          }
+        }
         p->h_units.push_back(u);
       }
     }

@@ -21,6 +21,7 @@ constexpr int kTmapBytes = 128;   // one CUtensorMap
 constexpr uint32_t kUnitFp8 = 1u;    // e4m3 codes + scale, else BF16 bytes
 constexpr uint32_t kUnitVec = 2u;    // rows are 16-byte aligned: bulk-copy path, else element path
 constexpr uint32_t kUnitMulti = 4u;  // block rows come from more than one shard
+constexpr uint32_t kUnitSliced = 8u; // some destination of the output takes a slice
 
 // Error word bits set by the kernel
 constexpr int32_t kErrBadStore = 1;  // debug checks: a store fell outside its pool range
@@ -63,6 +64,18 @@ struct DevDstPtr {
 };
 static_assert(sizeof(DevDstPtr) == 32, "layout");
 
+// Where the blocks of an output land in one destination (static). A block
+// (bi, bj) of the output is block (bi, bj) of a whole-tensor destination,
+// (map[bi], bj) of a row slice, (bi, map[bj]) of a column slice; a -1 map
+// entry means the destination does not hold that block row / column.
+struct DevDstGeom {
+  int32_t dim;         // -1 whole tensor, 0 row slice, 1 column slice
+  int32_t map_off;     // first entry of this destination's block map
+  uint32_t ld;         // elements per row of the destination tensor
+  uint32_t sld;        // scales per row of the destination's scale grid
+};
+static_assert(sizeof(DevDstGeom) == 16, "layout");
+
 // Everything one launch of the preparation kernel reads.
 struct PrepArgs {
   const DevUnit* units;
@@ -70,6 +83,8 @@ struct PrepArgs {
   const uint16_t* const* shard_ptrs;
   const unsigned char* tmaps;        // kTmapBytes per slot, 64-byte aligned
   const DevDstPtr* dst_ptrs;
+  const DevDstGeom* geom;            // per destination entry, like dst_ptrs
+  const int32_t* blockmap;
   int64_t unit_begin, unit_end;
   int32_t* error_word;               // kErr* bits
   uint64_t timeout_ns;               // limit of every wait inside the kernel
@@ -89,6 +104,10 @@ struct ParamInfo {
 struct DstInfo {
   int32_t rank = 0;
   uint64_t data_off = 0, scale_off = 0;
+  int32_t slice_dim = -1;                    // -1: the whole tensor
+  std::vector<int64_t> slice_begin, slice_len;
+  int64_t rows = 0, cols = 0;                // what this destination holds
+  uint64_t data_bytes = 0, scale_bytes = 0;
 };
 
 struct OutputInfo {
@@ -129,6 +148,8 @@ struct Plan {
   // host images of the static device tables
   std::vector<DevUnit> h_units;
   std::vector<DevRun> h_runs;
+  std::vector<DevDstGeom> h_geom;           // per destination entry
+  std::vector<int32_t> h_blockmap;
   // per slot: rows and cols of the shard, and whether a tensor map is
   // encoded for it (vec outputs, non-empty shards)
   std::vector<int64_t> slot_rows, slot_cols;

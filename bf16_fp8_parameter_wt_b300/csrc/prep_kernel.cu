@@ -341,6 +341,40 @@ __device__ __forceinline__ DevDstPtr load_dst(const PrepArgs& a, uint32_t i) {
   return d;
 }
 
+__device__ __forceinline__ uint4 ld_nc_v4(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+// Where block (bi, bj) lands in one destination: the element offset of the
+// thread's first row chunk, the element step between its rows, the index
+// of the block's scale, and whether the destination holds the block at all
+// (a tensor-parallel slice holds only some block rows or block columns).
+struct Place {
+  int64_t off, step;
+  uint32_t sidx;
+  bool held;
+};
+
+__device__ __forceinline__ Place place(const PrepArgs& a, const DevUnit& m, uint32_t entry, int r0, int cc) {
+  const uint32_t bi = m.bi, bj = m.bj;
+  // dim, map_off, ld, sld; an output without slices needs no table
+  const uint4 g = ((m.shape >> 16) & kUnitSliced)
+                      ? ld_nc_v4(a.geom + entry)
+                      : make_uint4(0xFFFFFFFFu, 0u, m.cols, (m.cols + kTile - 1) / kTile);
+  int32_t di = (int32_t)bi, dj = (int32_t)bj;
+  if ((int32_t)g.x == 0) di = (int32_t)ld_nc_u32(a.blockmap + (int32_t)g.y + bi);
+  else if ((int32_t)g.x == 1) dj = (int32_t)ld_nc_u32(a.blockmap + (int32_t)g.y + bj);
+  Place pl;
+  pl.held = di >= 0 && dj >= 0;
+  pl.off = ((int64_t)di * kTile + r0) * (int64_t)g.z + (int64_t)dj * kTile + cc * 8;
+  pl.step = kRowStride * (int64_t)g.z;
+  pl.sidx = (uint32_t)di * g.w + (uint32_t)dj;
+  return pl;
+}
+
 // Rows that are not 16-byte aligned: the group gathers the block element by
 // element into the stage (zeros outside the block), warp w taking rows
 // w, w + 4, ..., lanes taking consecutive columns. Eight rows are loaded
@@ -430,22 +464,23 @@ __device__ __forceinline__ void store_codes_bytes(const PrepArgs& a, const DevDs
 // every destination.
 template <bool kDebug>
 __device__ __noinline__ void store_fp8_general(const PrepArgs& a, const DevUnit m, const DevDstPtr dp0,
-                                               const uint8_t* tp, float s, int t, int r0, int cc,
-                                               int64_t row_off, int64_t row_step) {
+                                               const uint8_t* tp, float s, int t, int r0, int cc) {
   const int nrows = (int)(m.shape & 0xFFu) + 1, ncols = (int)((m.shape >> 8) & 0xFFu) + 1;
   const bool vec = (m.shape >> 16) & kUnitVec;
   const uint32_t se = (__float_as_uint(s) >> 23) & 0xFFu;
   const bool corr = se >= kMinScaleExp && se <= kMaxScaleExp;
   const float r = corr ? __frcp_rn(s) : 0.0f;
-  const uint32_t tiles_n = (m.cols + kTile - 1) / kTile;
   for (uint32_t d = 0; d < m.num_dsts; ++d) {
+    const Place pl = place(a, m, m.dst_begin + d, r0, cc);
+    if (!pl.held) continue;
     const DevDstPtr dp = d == 0 ? dp0 : load_dst<kDebug>(a, m.dst_begin + d);
     if (t == 0) {
-      float* sp4 = dp.scale + (uint64_t)m.bi * tiles_n + m.bj;
+      float* sp4 = dp.scale + pl.sidx;
       if (store_ok<kDebug>(a, dp, sp4, 4)) *sp4 = s;
     }
     if (cc * 8 >= ncols) continue;
-    uint8_t* row = dp.data + row_off;
+    uint8_t* row = dp.data + pl.off;
+    const int64_t row_step = pl.step;
 #pragma unroll 1
     for (int j = 0; j < kRows && r0 + kRowStride * j < nrows; ++j) {
       const uint4 v = *reinterpret_cast<const uint4*>(tp + j * kRowStride * kRowBytes);
@@ -463,14 +498,16 @@ __device__ __noinline__ void store_fp8_general(const PrepArgs& a, const DevUnit 
 // The general BF16 pass-through path, same cases.
 template <bool kDebug>
 __device__ __noinline__ void store_bf16_general(const PrepArgs& a, const DevUnit m, const DevDstPtr dp0,
-                                                const uint8_t* tp, int r0, int cc, int64_t row_off,
-                                                int64_t row_step) {
+                                                const uint8_t* tp, int r0, int cc) {
   const int nrows = (int)(m.shape & 0xFFu) + 1, ncols = (int)((m.shape >> 8) & 0xFFu) + 1;
   const bool vec = (m.shape >> 16) & kUnitVec;
   if (cc * 8 >= ncols) return;
   for (uint32_t d = 0; d < m.num_dsts; ++d) {
+    const Place pl = place(a, m, m.dst_begin + d, r0, cc);
+    if (!pl.held) continue;
     const DevDstPtr dp = d == 0 ? dp0 : load_dst<kDebug>(a, m.dst_begin + d);
-    uint8_t* row = dp.data + 2 * row_off;
+    uint8_t* row = dp.data + 2 * pl.off;
+    const int64_t row_step = pl.step;
 #pragma unroll 1
     for (int j = 0; j < kRows && r0 + kRowStride * j < nrows; ++j) {
       const uint4 v = *reinterpret_cast<const uint4*>(tp + j * kRowStride * kRowBytes);
@@ -508,6 +545,7 @@ __device__ void consumer(const PrepArgs& a, SmemCtl& sm, uint8_t* stages, int64_
       m = DevUnit{m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
     }
     const DevDstPtr dp0 = load_dst<kDebug>(a, m.dst_begin);
+    const Place pl0 = place(a, m, m.dst_begin, r0, cc);
     const uint32_t flags = m.shape >> 16;
     const int nrows = (int)(m.shape & 0xFFu) + 1, ncols = (int)((m.shape >> 8) & 0xFFu) + 1;
     const bool whole = (m.shape & 0xFFFFu) == 0x7F7Fu;
@@ -531,13 +569,9 @@ __device__ void consumer(const PrepArgs& a, SmemCtl& sm, uint8_t* stages, int64_
           v[j] = *reinterpret_cast<const uint4*>(tp + j * kRowStride * kRowBytes);
       }
     }
-    const int64_t N = m.cols;
-    const int64_t row_off = ((int64_t)m.bi * kTile + r0) * N + (int64_t)m.bj * kTile + cc * 8;
-    const int64_t row_step = kRowStride * N;
-
     // the common case runs straight through: a whole block of 16-byte rows
     // with one destination; everything else takes the general routines
-    const bool fast = !kDebug && whole && vec && m.num_dsts == 1;
+    const bool fast = !kDebug && whole && vec && m.num_dsts == 1 && pl0.held;
     const uint32_t empty = smem_u32(&sm.empty[st]);
 
     if (flags & kUnitFp8) {
@@ -568,21 +602,21 @@ __device__ void consumer(const PrepArgs& a, SmemCtl& sm, uint8_t* stages, int64_
 #pragma unroll
         for (int j = 0; j < kRows; ++j) q[j] = quant_chunk(v[j], s, r);
         mbar_arrive(empty);                       // the codes are in registers
-        if (t == 0) dp0.scale[(uint64_t)m.bi * ((m.cols + kTile - 1) / kTile) + m.bj] = s;
-        uint8_t* row = dp0.data + row_off;
+        if (t == 0) dp0.scale[pl0.sidx] = s;
+        uint8_t* row = dp0.data + pl0.off;
 #pragma unroll
-        for (int j = 0; j < kRows; ++j) *reinterpret_cast<uint2*>(row + j * row_step) = q[j];
+        for (int j = 0; j < kRows; ++j) *reinterpret_cast<uint2*>(row + j * pl0.step) = q[j];
       } else {
-        store_fp8_general<kDebug>(a, m, dp0, tp, s, t, r0, cc, row_off, row_step);
+        store_fp8_general<kDebug>(a, m, dp0, tp, s, t, r0, cc);
         mbar_arrive(empty);
       }
     } else if (fast) {
       mbar_arrive(empty);                         // the block is in registers
-      uint8_t* row = dp0.data + 2 * row_off;
+      uint8_t* row = dp0.data + 2 * pl0.off;
 #pragma unroll
-      for (int j = 0; j < kRows; ++j) *reinterpret_cast<uint4*>(row + 2 * j * row_step) = v[j];
+      for (int j = 0; j < kRows; ++j) *reinterpret_cast<uint4*>(row + 2 * j * pl0.step) = v[j];
     } else {
-      store_bf16_general<kDebug>(a, m, dp0, tp, r0, cc, row_off, row_step);
+      store_bf16_general<kDebug>(a, m, dp0, tp, r0, cc);
       mbar_arrive(empty);
     }
   }

@@ -44,11 +44,17 @@ class wt_param_desc(C.Structure):
                 ("num_shards", C.c_int32), ("shard_rows", C.POINTER(C.c_int64))]
 
 
+class wt_slice_desc(C.Structure):
+    _fields_ = [("dim", C.c_int32), ("num_ranges", C.c_int32),
+                ("begin", C.POINTER(C.c_int64)), ("length", C.POINTER(C.c_int64))]
+
+
 class wt_output_desc(C.Structure):
     _fields_ = [("name", C.c_char_p), ("num_parts", C.c_int32),
                 ("part_params", C.POINTER(C.c_int32)), ("format", C.c_int32),
                 ("num_dsts", C.c_int32), ("dst_ranks", C.POINTER(C.c_int32)),
-                ("dst_data_off", C.POINTER(C.c_uint64)), ("dst_scale_off", C.POINTER(C.c_uint64))]
+                ("dst_data_off", C.POINTER(C.c_uint64)), ("dst_scale_off", C.POINTER(C.c_uint64)),
+                ("dst_slices", C.POINTER(wt_slice_desc))]
 
 
 class wt_plan_desc(C.Structure):
@@ -115,7 +121,8 @@ def _ptr_array(ptrs: Sequence[int]):
 class PlanDesc:
     """A wt_plan_desc built from a workload-like object: .params (name,
     rows, cols, shard_rows), .outputs (name, parts, fp8, dst_ranks,
-    data_off, scale_off; None offsets = automatic) and .num_ranks."""
+    data_off, scale_off; None offsets = automatic; slices: None or per
+    destination None / (dim, ((begin, length), ...))) and .num_ranks."""
 
     def __init__(self, w, pool_capacity: Optional[Sequence[int]] = None,
                  offload_chunk_bytes: int = 0, flags: int = 0):
@@ -141,9 +148,22 @@ class PlanDesc:
                 soff = (C.c_uint64 * len(o.scale_off))(
                     *[WT_OFFSET_AUTO if v is None else v for v in o.scale_off])
                 keep.append(soff)
+            slices = None
+            if getattr(o, "slices", None) is not None:
+                slices = (wt_slice_desc * max(1, len(o.slices)))()
+                for d, sl in enumerate(o.slices):
+                    if sl is None:
+                        slices[d] = wt_slice_desc(0, 0, None, None)
+                        continue
+                    dim, ranges = sl
+                    b = (C.c_int64 * max(1, len(ranges)))(*[r[0] for r in ranges])
+                    n = (C.c_int64 * max(1, len(ranges)))(*[r[1] for r in ranges])
+                    keep += [b, n]
+                    slices[d] = wt_slice_desc(dim, len(ranges), b, n)
+                keep.append(slices)
             fmt = WT_OUT_FP8_E4M3_B128 if o.fp8 else WT_OUT_BF16
             outs[i] = wt_output_desc(name, len(o.parts), parts, fmt, len(o.dst_ranks), ranks,
-                                     doff, soff)
+                                     doff, soff, slices)
         cap = None
         if pool_capacity is not None:
             cap = (C.c_uint64 * max(1, len(pool_capacity)))(*pool_capacity)

@@ -77,6 +77,24 @@ typedef struct {
   const int64_t* shard_rows;
 } wt_param_desc;
 
+/* The part of an output that one destination takes, for tensor-parallel
+ * inference layouts (the pages map 256 training GPUs onto 128 inference
+ * GPUs, each holding its shard of every layer): the listed row ranges
+ * (dim 0: column-parallel layers such as qkv or gate_up, one range per
+ * fusion part) or column ranges (dim 1: row-parallel layers such as o or
+ * down) of the fused tensor, concatenated in order. The destination holds
+ * that tensor (row-major, no padding) and, for FP8, the matching block rows
+ * or block columns of the scale grid. Every range starts at a multiple of
+ * 128 and is a multiple of 128 long, except that the last range may end at
+ * the tensor's edge; ranges do not overlap. num_ranges == 0: the whole
+ * tensor. */
+typedef struct {
+  int32_t dim;              /* 0: rows, 1: columns */
+  int32_t num_ranges;
+  const int64_t* begin;     /* first row / column of each range */
+  const int64_t* length;    /* rows / columns of each range */
+} wt_slice_desc;
+
 /* One output tensor: the row concatenation of part_params in that order
  * (projection fusion: q,k,v -> qkv; gate,up -> gate_up), written in
  * `format` to each of num_dsts destinations (rank, data offset, scale
@@ -84,7 +102,10 @@ typedef struct {
  * WT_OFFSET_AUTO entries. Explicit data offsets must be multiples of 16,
  * explicit scale offsets multiples of 4.
  *
- * Destination layout of an output of M x N:
+ * dst_slices may be NULL (every destination takes the whole tensor) or hold
+ * one wt_slice_desc per destination.
+ *
+ * Destination layout of an output (or slice) of M x N:
  *   FP8 : M*N code bytes, row-major, no padding inside the tensor, at
  *         data_off; ceil(M/128) x ceil(N/128) fp32 scales, row-major,
  *         little-endian, at scale_off. Blocks are aligned to the fused
@@ -103,6 +124,7 @@ typedef struct {
   const int32_t* dst_ranks;
   const uint64_t* dst_data_off;
   const uint64_t* dst_scale_off;
+  const wt_slice_desc* dst_slices;
 } wt_output_desc;
 
 /* The whole static schedule. Every param must be used by exactly one

@@ -9,7 +9,7 @@ import pytest
 import bf16_fp8_parameter_wt_b300 as wt
 from bf16_fp8_parameter_wt_b300 import build as wt_build
 from workloads import (Output, Param, ValueRecipe, Workload, edge_stress, kimi_k2_moe_layer,
-                       llama_dense, offload_layer, tiny_dense)
+                       llama_dense, llama_dense_tp4, offload_layer, tiny_dense, tp_slices_small)
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
@@ -41,7 +41,7 @@ def test_status_strings():
 
 
 @pytest.mark.parametrize("make", [tiny_dense, llama_dense, kimi_k2_moe_layer, edge_stress,
-                                  lambda: offload_layer(4)])
+                                  lambda: offload_layer(4), llama_dense_tp4, tp_slices_small])
 def test_host_plan_layout_equals_oracle(oracle_mod, make):
     w = make()
     d, s, pools = oracle_mod.Model(w).layout()
@@ -167,3 +167,30 @@ def test_testing_hooks_validate_their_arguments():
             assert ei.value.name == "WT_ERR_INVALID_ARGUMENT"
         wt.wt_debug_stall_unit(p.handle, n - 1, 1000)
         wt.wt_debug_stall_unit(p.handle, -1, 0)
+
+
+@pytest.mark.parametrize("sl,status", [((0, ((64, 128),)), "WT_ERR_SHAPE"),
+                                       ((0, ((0, 100), (128, 128))), "WT_ERR_SHAPE"),
+                                       ((0, ((0, 256), (128, 128))), "WT_ERR_SHAPE"),
+                                       ((0, ((256, 128),)), "WT_ERR_SHAPE"),
+                                       ((1, ((0, 200),)), "WT_ERR_SHAPE"),
+                                       ((2, ((0, 128),)), "WT_ERR_INVALID_ARGUMENT"),
+                                       ((0, ((0, 0),)), "WT_ERR_SHAPE")])
+def test_invalid_slices_are_rejected(sl, status):
+    w = Workload("bad", [Param("p", 300, 260, (300,))],
+                 [Output("p", (0,), True, (0,), slices=(sl,))], 1)
+    with pytest.raises(wt.WTError) as ei:
+        wt.Plan(w, device=-1)
+    assert ei.value.name == status
+
+
+def test_tensor_parallel_blocks_have_one_destination():
+    """Every block of a sliced Linear layer of the TP stack goes to exactly
+    one rank: the pool sizes add up to the unsliced tensors once, plus the
+    replicated norms."""
+    w = llama_dense_tp4()
+    with wt.Plan(w, device=-1) as p:
+        assert p.stats["bytes_written"] == w.bytes_written
+    one = llama_dense()
+    norms = sum(2 * 4096 for o in one.outputs if o.name.endswith("norm"))
+    assert w.bytes_written == one.bytes_written + 3 * norms

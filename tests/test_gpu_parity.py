@@ -9,7 +9,8 @@ import bf16_fp8_parameter_wt_b300 as wt
 from gpu_helpers import (CANARY, assert_pools_equal, device_pools, full_check, ncores,
                          oracle_pools, run_gpu)
 from workloads import (Output, Param, ValueRecipe, Workload, edge_stress, kimi_k2_moe_layer,
-                       llama_dense, make_shards, shards_to_host_u16, tiny_dense)
+                       llama_dense, llama_dense_tp4, make_shards, shards_to_host_u16, tiny_dense,
+                       tp_slices_small)
 
 pytestmark = pytest.mark.gpu
 
@@ -43,6 +44,27 @@ def test_llama_dense_full(oracle_mod):
 
 def test_edge_stress_full(oracle_mod):
     full_check(oracle_mod, edge_stress())
+
+
+def test_tensor_parallel_slices_small(oracle_mod):
+    """Row and column slices, in and out of order, ending at the edge,
+    mixed with whole-tensor destinations and replicas; through the single-
+    destination fast path, the general path, the element path and the
+    debug-checked kernel."""
+    w = tp_slices_small()
+    shards = make_shards(w, device="cuda:0")
+    want = oracle_pools(oracle_mod, w, shards)
+    for flags in (0, wt.WT_FLAG_FORCE_NARROW, wt.WT_FLAG_DEBUG_CHECKS):
+        plan, pools = run_gpu(w, shards, flags=flags)
+        plan.check()
+        assert_pools_equal(pools, want)
+        plan.close()
+
+
+def test_llama_dense_tp4_full(oracle_mod):
+    """The Llama-style stack laid out for 4-way tensor parallelism: every
+    Linear layer sliced per rank, norms replicated."""
+    full_check(oracle_mod, llama_dense_tp4())
 
 
 def test_small_shapes_and_special_values(oracle_mod):

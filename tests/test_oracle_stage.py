@@ -7,7 +7,7 @@ import torch
 
 import bruteforce as bf
 from workloads import Output, Param, ValueRecipe, Workload, make_shards, shards_to_host_u16
-from workloads import edge_stress, kimi_k2_moe_layer, llama_dense, tiny_dense
+from workloads import edge_stress, kimi_k2_moe_layer, llama_dense, tiny_dense, tp_slices_small
 
 
 # --------------------------------------------------------------------------
@@ -253,20 +253,6 @@ def test_prepare_covers_every_scheduled_byte_once(oracle_mod):
 # tensor-parallel destination slices
 # --------------------------------------------------------------------------
 
-def _sliced_workload():
-    """An FP8 output fused from two parts (300 x 260: partial blocks in both
-    dimensions) and a BF16 output, each sent whole and as row / column
-    slices, in and out of order, including ranges that end at the edge."""
-    params = [Param("a1", 172, 260, (100, 72)), Param("a2", 128, 260, (128,)),
-              Param("b", 200, 136, (64, 136))]
-    fp8_slices = (None, (0, ((128, 128), (0, 128))), (0, ((256, 44),)),
-                  (1, ((128, 132),)), (1, ((0, 128), (256, 4))))
-    bf16_slices = (None, (0, ((0, 128), (128, 72))), (1, ((128, 8),)))
-    outs = [Output("a", (0, 1), True, (0, 1, 0, 1, 0), slices=fp8_slices),
-            Output("b", (2,), False, (1, 0, 1), slices=bf16_slices)]
-    return Workload("sliced", params, outs, 2, ValueRecipe("student_t3", 0.02, 41))
-
-
 def _expected_slice(data, scales, shape, sl, fp8):
     """numpy slicing of a whole prepared output (codes and block scales)."""
     m, n = shape
@@ -287,7 +273,7 @@ def _expected_slice(data, scales, shape, sl, fp8):
 
 
 def test_slices_equal_numpy_slicing_of_the_whole_output(oracle_mod):
-    w = _sliced_workload()
+    w = tp_slices_small()
     flat = shards_to_host_u16(make_shards(w))
     m = oracle_mod.Model(w)
     pools = m.prepare(flat, nthreads=2)

@@ -14,7 +14,8 @@ import pytest
 import torch
 
 import bf16_fp8_parameter_wt_b300 as wt
-from workloads import Output, Param, ValueRecipe, Workload, kimi_k2_moe_layer, make_shards, tiny_dense
+from workloads import (Output, Param, ValueRecipe, Workload, kimi_k2_moe_layer, make_shards,
+                       tiny_dense, tp_slices_small)
 
 pytestmark = pytest.mark.gpu
 
@@ -44,7 +45,7 @@ def _small_shapes():
     return Workload("noalloc_small", params, outs, 2, ValueRecipe("student_t3", 0.02, 31))
 
 
-@pytest.mark.parametrize("make", [tiny_dense, _small_shapes])
+@pytest.mark.parametrize("make", [tiny_dense, _small_shapes, tp_slices_small])
 def test_noalloc_matches_prepare_on_two_calls(make):
     w = make()
     shards = make_shards(w, device="cuda:0")
@@ -58,10 +59,10 @@ def test_noalloc_matches_prepare_on_two_calls(make):
     # which pool bytes the schedule writes (the rest is alignment padding)
     masks = [np.zeros(plan.pool_bytes(r) + 256, bool) for r in range(w.num_ranks)]
     for o, out in enumerate(w.outputs):
-        m_, n_ = w.output_shape(o)
-        data = m_ * n_ * (1 if out.fp8 else 2)
-        scales = 4 * (-(-m_ // 128)) * (-(-n_ // 128)) if out.fp8 else 0
         for k in range(len(out.dst_ranks)):
+            m_, n_ = w.dst_shape(o, k)
+            data = m_ * n_ * (1 if out.fp8 else 2)
+            scales = 4 * (-(-m_ // 128)) * (-(-n_ // 128)) if out.fp8 else 0
             rank, doff, soff = plan.output_layout(o, k)
             masks[rank][doff:doff + data] = True
             masks[rank][soff:soff + scales] = True

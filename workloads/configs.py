@@ -156,9 +156,9 @@ class _Builder:
         self.w.params.append(Param(name, rows, cols, tuple(sr)))
         return len(self.w.params) - 1
 
-    def output(self, name, parts, fp8, dst_ranks, data_off=None, scale_off=None):
+    def output(self, name, parts, fp8, dst_ranks, data_off=None, scale_off=None, slices=None):
         self.w.outputs.append(Output(name, tuple(parts), fp8, tuple(dst_ranks),
-                                     data_off, scale_off))
+                                     data_off, scale_off, slices))
 
     def round_robin_rank(self):
         """Outputs go round-robin over the ranks in plan order."""
@@ -206,6 +206,86 @@ def llama_dense(lm_head_fp8=True) -> Workload:
     return dense_transformer("llama_dense_4l_h4096", 4, 4096, 32, 8, 128, 14336, 128256,
                              shards=8, ranks=4, values=ValueRecipe("normal", 0.02, 1002),
                              lm_head_fp8=lm_head_fp8)
+
+
+def tp_split(extent: int, tp: int) -> list:
+    """(begin, length) of each of tp 128-aligned pieces covering [0, extent):
+    ceil(extent / tp) rounded up to 128 each, the remainder last."""
+    per = -(-(-(-extent // tp)) // TILE) * TILE
+    out, b = [], 0
+    for _ in range(tp):
+        n = max(0, min(per, extent - b))
+        out.append((b, n))
+        b += n
+    return out
+
+
+def dense_transformer_tp(name, layers, hidden, q_heads, kv_heads, head_dim, ffn, vocab,
+                         shards, tp, values) -> Workload:
+    """The dense stack of dense_transformer laid out for tensor-parallel
+    inference on tp ranks: every rank takes its slice of every Linear layer
+    (column-parallel qkv and gate_up: its heads / its FFN rows of each
+    fusion part; row-parallel o and down: its input columns), the
+    vocabulary-parallel embedding and lm_head are split along rows, and the
+    norms are replicated. Every 128x128 block of a sliced tensor goes to
+    exactly one rank."""
+    b = _Builder(name, tp, shards, values)
+    ranks = tuple(range(tp))
+
+    def rows_of(parts_rows):
+        """Per rank, its row range of each fusion part, as fused-row ranges."""
+        per_rank = [[] for _ in range(tp)]
+        base = 0
+        for n in parts_rows:
+            for r, (bg, ln) in enumerate(tp_split(n, tp)):
+                if ln:
+                    per_rank[r].append((base + bg, ln))
+            base += n
+        return tuple((0, tuple(x)) for x in per_rank)
+
+    def cols_of(n):
+        return tuple((1, (rng,)) for rng in tp_split(n, tp))
+
+    b.output("embed", [b.param("embed", vocab, hidden)], False, ranks, slices=rows_of([vocab]))
+    qd, kvd = q_heads * head_dim, kv_heads * head_dim
+    for l in range(layers):
+        q = b.param(f"l{l}.q", qd, hidden)
+        k = b.param(f"l{l}.k", kvd, hidden)
+        v = b.param(f"l{l}.v", kvd, hidden)
+        b.output(f"l{l}.qkv", [q, k, v], True, ranks, slices=rows_of([qd, kvd, kvd]))
+        b.output(f"l{l}.o", [b.param(f"l{l}.o", hidden, qd)], True, ranks, slices=cols_of(qd))
+        g = b.param(f"l{l}.gate", ffn, hidden)
+        u = b.param(f"l{l}.up", ffn, hidden)
+        b.output(f"l{l}.gate_up", [g, u], True, ranks, slices=rows_of([ffn, ffn]))
+        b.output(f"l{l}.down", [b.param(f"l{l}.down", hidden, ffn)], True, ranks,
+                 slices=cols_of(ffn))
+        b.output(f"l{l}.attn_norm", [b.param(f"l{l}.attn_norm", hidden, 1)], False, ranks)
+        b.output(f"l{l}.mlp_norm", [b.param(f"l{l}.mlp_norm", hidden, 1)], False, ranks)
+    b.output("final_norm", [b.param("final_norm", hidden, 1)], False, ranks)
+    b.output("lm_head", [b.param("lm_head", vocab, hidden)], True, ranks, slices=rows_of([vocab]))
+    return b.w
+
+
+def tp_slices_small() -> Workload:
+    """Small slicing cases: an FP8 output fused from two parts (300 x 260,
+    partial blocks in both dimensions) and a BF16 output (200 x 136), each
+    sent whole and as row / column slices, in and out of order, with ranges
+    that end at the tensor's edge, replicated on two ranks."""
+    params = [Param("a1", 172, 260, (100, 72)), Param("a2", 128, 260, (128,)),
+              Param("b", 200, 136, (64, 136))]
+    fp8_slices = (None, (0, ((128, 128), (0, 128))), (0, ((256, 44),)),
+                  (1, ((128, 132),)), (1, ((0, 128), (256, 4))))
+    bf16_slices = (None, (0, ((0, 128), (128, 72))), (1, ((128, 8),)))
+    outs = [Output("a", (0, 1), True, (0, 1, 0, 1, 0), slices=fp8_slices),
+            Output("b", (2,), False, (1, 0, 1), slices=bf16_slices)]
+    return Workload("tp_slices_small", params, outs, 2, ValueRecipe("student_t3", 0.02, 41))
+
+
+def llama_dense_tp4() -> Workload:
+    """The four-layer Llama-style stack of llama_dense, laid out for 4-way
+    tensor-parallel inference (see dense_transformer_tp)."""
+    return dense_transformer_tp("llama_dense_4l_h4096_tp4", 4, 4096, 32, 8, 128, 14336, 128256,
+                                shards=8, tp=4, values=ValueRecipe("normal", 0.02, 1002))
 
 
 def _moe_experts(b: _Builder, prefix: str, experts: int, hidden: int, inter: int,
@@ -261,6 +341,8 @@ def offload_layer(experts: int = 385, seed: int = 1005) -> Workload:
 WORKLOADS = {
     "tiny_dense": tiny_dense,
     "llama_dense": llama_dense,
+    "llama_dense_tp4": llama_dense_tp4,
+    "tp_slices_small": tp_slices_small,
     "kimi_k2_moe_layer": kimi_k2_moe_layer,
     "edge_stress": edge_stress,
     "offload_layer": offload_layer,
