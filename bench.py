@@ -265,6 +265,7 @@ def main():
     pools = [torch.empty(max(1, plan.pool_bytes(r)), dtype=torch.uint8, device=dev)
              for r in range(w.num_ranks)]
     pool_ptrs = [p.data_ptr() for p in pools]
+    shard_ptrs, pool_ptrs = plan.bind(shard_ptrs, pool_ptrs)
     stream = torch.cuda.Stream(dev)
     sp = stream.cuda_stream
 

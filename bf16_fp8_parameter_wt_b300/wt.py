@@ -111,7 +111,11 @@ def _check(status: int) -> None:
         raise WTError(status, lib().wt_last_error().decode(errors="replace"))
 
 
-def _ptr_array(ptrs: Sequence[int]):
+def _ptr_array(ptrs):
+    """A C array of device pointers; an array that is already one (see
+    Plan.bind) is passed through without copying."""
+    if isinstance(ptrs, C.Array):
+        return ptrs
     arr = (C.c_void_p * max(1, len(ptrs)))()
     for i, p in enumerate(ptrs):
         arr[i] = int(p) if p else None
@@ -270,6 +274,12 @@ class Plan:
     @property
     def stats(self) -> dict:
         return wt_plan_get_stats(self.handle)
+
+    def bind(self, shard_ptrs, pools) -> tuple:
+        """The pointer arrays of one set of buffers, built once: passing the
+        result to prepare (as prepare(*plan.bind(...), stream)) skips the
+        per-call conversion of thousands of Python integers."""
+        return _ptr_array(shard_ptrs), _ptr_array(pools)
 
     def prepare(self, shard_ptrs, pools, stream: int = 0) -> None:
         wt_prepare(self.handle, shard_ptrs, pools, stream)

@@ -85,6 +85,8 @@ def lib():
                                         C.c_void_p]
         L.wo_prepare.argtypes = [C.POINTER(_Model), C.c_void_p, C.c_void_p, C.c_void_p,
                                  C.c_void_p, C.c_int32]
+        L.wo_quantize_tokens.argtypes = [C.c_void_p, C.c_int64, C.c_int64, C.c_int64,
+                                         C.c_void_p, C.c_void_p]
         _lib = L
     return _lib
 
@@ -116,6 +118,21 @@ def tile_scale(amax: float) -> np.float32:
 
 def quantize_element(x_bits: int, s) -> int:
     return lib().wo_quantize_element(int(x_bits), float(np.float32(s)))
+
+
+def quantize_tokens(x_bits: np.ndarray, hidden: int = None):
+    """(codes, scales) of the 1 x 128 activation codec for a 2-D uint16 BF16
+    array (rows are tokens; a strided view is honoured through its row
+    stride)."""
+    assert x_bits.dtype == np.uint16 and x_bits.ndim == 2 and x_bits.strides[1] == 2
+    tokens, h = x_bits.shape
+    hidden = h if hidden is None else hidden
+    ld = x_bits.strides[0] // 2
+    codes = np.empty((tokens, hidden), np.uint8)
+    scales = np.empty((tokens, -(-hidden // 128)), np.float32)
+    lib().wo_quantize_tokens(x_bits.ctypes.data, tokens, hidden, ld, codes.ctypes.data,
+                             scales.ctypes.data)
+    return codes, scales
 
 
 # --------------------------------------------------------------------------

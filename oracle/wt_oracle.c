@@ -372,6 +372,26 @@ static void copy_slice(const wo_output* out, const wo_slice* sl, int64_t rows, i
   }
 }
 
+/* READING (activation codec): the dispatch kernels quantise each token's
+ * hidden vector in groups of 128 channels ("block-scaled fp8 dispatch",
+ * hidden 7168); the scale and code are those of the weight blocks. */
+void wo_quantize_tokens(const uint16_t* x, int64_t tokens, int64_t hidden, int64_t ld,
+                        uint8_t* codes, float* scales) {
+  const int64_t groups = ceil_div(hidden, TILE);
+  for (int64_t t = 0; t < tokens; ++t)
+    for (int64_t g = 0; g < groups; ++g) {
+      const int64_t c0 = g * TILE, c1 = c0 + TILE < hidden ? c0 + TILE : hidden;
+      float amax = 0.0f;
+      for (int64_t c = c0; c < c1; ++c) {
+        float a = fabsf(wo_bf16_value(x[t * ld + c]));
+        if (a > amax) amax = a;
+      }
+      const float s = wo_tile_scale(amax);
+      scales[t * groups + g] = s;
+      for (int64_t c = c0; c < c1; ++c) codes[t * hidden + c] = wo_quantize_element(x[t * ld + c], s);
+    }
+}
+
 typedef struct {
   const wo_model* m;
   const uint64_t* data_off;

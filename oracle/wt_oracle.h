@@ -26,6 +26,8 @@
  *       offsets; slices against numpy slicing of the whole output.
  *   wo_prepare_output / wo_prepare : torch.cat of the shards (reassembly and
  *       fusion), numpy amax, exact-rational brute force on tiny tensors.
+ *   wo_quantize_tokens : exact-rational brute force per group, the
+ *       dequantisation error bound, power-of-two scaling invariance.
  */
 #ifndef WT_ORACLE_H
 #define WT_ORACLE_H
@@ -118,6 +120,15 @@ int wo_layout(const wo_model* m, uint64_t* data_off, uint64_t* scale_off,
 int wo_prepare_output(const wo_model* m, int32_t o,
                       const uint16_t* const* shards, uint8_t* data_out,
                       float* scale_out);
+
+/* The activation codec of the MoE dispatch (the same e4m3 arithmetic at
+ * 1 x 128 granularity): x is tokens x hidden BF16 with a row stride of ld
+ * elements; for each token and each group of 128 consecutive channels (the
+ * last group may be shorter), scale = amax / 448 (1.0 for an all-zero
+ * group) and code = E(fl32(x / scale)). codes: tokens x hidden bytes,
+ * row-major; scales: tokens x ceil(hidden / 128) floats, row-major. */
+void wo_quantize_tokens(const uint16_t* x, int64_t tokens, int64_t hidden, int64_t ld,
+                        uint8_t* codes, float* scales);
 
 /* The whole stage into host pools at the given (resolved) offsets, using
  * nthreads worker threads over outputs. */

@@ -110,3 +110,19 @@ def quantize_matrix(bits, rows: int, cols: int):
             for i in idx:
                 codes[i] = element_code(bits[i], s)
     return codes, scales
+
+
+def quantize_rows(bits, rows: int, cols: int):
+    """Codes (row-major list) and per-row group scales (list of Fractions,
+    row-major, ceil(cols/128) per row) of the 1 x 128 activation codec."""
+    codes = [0] * (rows * cols)
+    scales = []
+    for r in range(rows):
+        for c0 in range(0, cols, 128):
+            idx = [r * cols + c for c in range(c0, min(c0 + 128, cols))]
+            amax = max(abs(bf16_value(bits[i])) for i in idx)
+            s = block_scale(amax)
+            scales.append(s)
+            for i in idx:
+                codes[i] = element_code(bits[i], s)
+    return codes, scales
