@@ -228,7 +228,9 @@ def main():
     ap.add_argument("--reference-experts", type=int, default=2)
     ap.add_argument("--workload", default="kimi_k2_moe_layer",
                     choices=["kimi_k2_moe_layer", "llama_dense", "llama_dense_tp4", "edge_stress",
-                             "tiny_dense", "offload_8layer"])
+                             "tiny_dense", "offload_8layer", "tokens"])
+    ap.add_argument("--tokens", type=int, default=131072)
+    ap.add_argument("--hidden", type=int, default=7168)
     ap.add_argument("--images", type=int, default=2)
     ap.add_argument("--stack-steps", type=int, default=2)
     ap.add_argument("--stack-warmup", type=int, default=1)
@@ -243,6 +245,9 @@ def main():
         return
     if args.workload == "offload_8layer":
         run_offload_stack(args, world, rank, local)
+        return
+    if args.workload == "tokens":
+        run_tokens(args, world, rank, local)
         return
 
     import torch
@@ -352,6 +357,90 @@ def main():
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+def run_tokens(args, world, rank, local):
+    """The 1 x 128 activation codec (wt_quantize_tokens) on a dispatch-shaped
+    batch: --tokens x --hidden BF16 (Student-t(3) x 0.02), codes and scales
+    written to device buffers; the large default batch (1.9 GB) is larger
+    than L2, a 128-token batch gives the per-dispatch latency."""
+    import torch
+    import bf16_fp8_parameter_wt_b300 as wt
+    from bf16_fp8_parameter_wt_b300 import build as wt_build
+    wt_build.build()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    T, H = args.tokens, args.hidden
+    G = -(-H // 128)
+    g = torch.Generator(device=dev).manual_seed(1006 + rank)
+    z = torch.randn(T, H, generator=g, device=dev)
+    chi = sum(torch.randn(T, H, generator=g, device=dev) ** 2 for _ in range(3))
+    x = (z.mul_(0.02).div_(chi.div_(3).sqrt_())).to(torch.bfloat16)
+    del z, chi
+    codes = torch.empty(T, H, dtype=torch.uint8, device=dev)
+    scales = torch.empty(T, G, dtype=torch.float32, device=dev)
+    stream = torch.cuda.Stream(dev)
+
+    def step():
+        wt.wt_quantize_tokens(x.data_ptr(), T, H, H, codes.data_ptr(), scales.data_ptr(),
+                              stream.cuda_stream)
+
+    for _ in range(args.warmup):
+        step()
+    stream.synchronize()
+    small = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    clocks = ClockSampler(None)
+    time.sleep(0.3)
+    for i in range(args.steps):
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    stream.synchronize()
+    clk = clocks.stop()
+    per = [s_.elapsed_time(e_) for s_, e_ in zip(starts, ends)]
+    ms = max_over_ranks(world, starts[0].elapsed_time(ends[-1]) / args.steps, dev)
+    # one dispatch-sized call (128 tokens), latency only: captured in a CUDA
+    # graph so that the replay times the kernel and its launch, not the
+    # Python call around it
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        wt.wt_quantize_tokens(x.data_ptr(), 128, H, H, codes.data_ptr(), scales.data_ptr(),
+                              stream.cuda_stream)
+    for _ in range(3):
+        graph.replay()
+    stream.synchronize()
+    reps = 20
+    small[0].record(stream)
+    for _ in range(reps):
+        graph.replay()
+    small[1].record(stream)
+    stream.synchronize()
+    bytes_in = 2 * T * H
+    alg = bytes_in + T * H + 4 * T * G
+    peak = measured_peaks().get("hbm_gbs") or 6400.0
+    achieved = alg / (statistics.mean(per) * 1e-3) / 1e9
+    line = {
+        "metric": "wt_quantize_tokens GB/s (BF16 in), 1x128 e4m3 activation codec",
+        "value": round(world * bytes_in / (ms * 1e-3) / 1e9, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded Student-t(3) x 0.02 BF16, generated on device)",
+        "config": {"workload": f"tokens_{T}x{H}", "tokens": T, "hidden": H,
+                   "l2": "inputs larger than the 126 MB L2, no flush" if bytes_in > L2_BYTES else
+                         "inputs smaller than L2"},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "frac_of_8TBs_spec": round(achieved / SPEC_HBM_GBS, 4),
+                     "algorithmic_bytes_per_launch": alg, "kernel": "token_kernel",
+                     "launch_ms_median": round(statistics.median(per), 4)},
+        "dispatch_128_tokens_us": round(small[0].elapsed_time(small[1]) * 1e3 / reps, 2),
+        "clocks": clk, "gpu_launches": args.steps,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
 
 
 def pinned_image(plan, shards):

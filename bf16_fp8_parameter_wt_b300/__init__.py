@@ -6,7 +6,7 @@ from .wt import (EXPORTS, LIB_PATH, WT_FLAG_DEBUG_CHECKS, WT_FLAG_FORCE_NARROW, 
                  WT_OUT_BF16, WT_OUT_FP8_E4M3_B128, Plan, PlanDesc, WTError, lib,
                  wt_debug_fail_offload_chunk, wt_debug_stall_unit, wt_last_error, wt_plan_check, wt_plan_create,
                  wt_plan_destroy, wt_plan_get_stats, wt_plan_output_layout, wt_plan_pool_bytes,
-                 wt_plan_shard_host_offset, wt_prepare, wt_prepare_noalloc, wt_prepare_offload,
+                 wt_plan_shard_host_offset, wt_prepare, wt_prepare_noalloc, wt_prepare_offload, wt_quantize_tokens,
                  wt_status_string)
 
 __all__ = [
@@ -14,6 +14,6 @@ __all__ = [
     "WT_OUT_BF16", "WT_OUT_FP8_E4M3_B128", "Plan", "PlanDesc", "WTError", "lib",
     "wt_debug_fail_offload_chunk", "wt_debug_stall_unit", "wt_last_error", "wt_plan_check", "wt_plan_create",
     "wt_plan_destroy", "wt_plan_get_stats", "wt_plan_output_layout", "wt_plan_pool_bytes",
-    "wt_plan_shard_host_offset", "wt_prepare", "wt_prepare_noalloc", "wt_prepare_offload",
+    "wt_plan_shard_host_offset", "wt_prepare", "wt_prepare_noalloc", "wt_prepare_offload", "wt_quantize_tokens",
     "wt_status_string",
 ]

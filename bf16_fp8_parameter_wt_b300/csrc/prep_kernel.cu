@@ -33,30 +33,14 @@
 //     re-read the thread's rows from the stage before releasing it, so
 //     their code stays out of the hot path's registers.
 //
-// Division. The code of x must be E(fl32(x / s)). The scale is the same for
-// the whole block, so the kernel forms r = RN(1/s) once and gets each
-// quotient with one reciprocal-based correction step (Markstein):
-//   q0 = RN(x r),  e = x - q0 s (one fma),  y = fma(e, r, q0).
-// q0 is within one ulp of x/s, so the remainder e = x - q0 s is exact, and
-// y = RN(x/s + (x/s - q0) d) where d, the relative error of r, is at most
-// 2^-24: y differs from fl32(x/s) only if x/s lies within 2^-47 (relative)
-// of a binary32 rounding boundary without being on it. x/s can never sit
-// exactly on such a boundary (x has 8 significant bits, s 24), and exact
-// e4m3 ties (x/s equal to an e4m3 midpoint, which BF16 inputs hit often)
-// are binary32 numbers, which the correction reproduces exactly. Whether a
-// near-boundary quotient exists is settled by the GPU test that runs every
-// pair (block amax, element) of BF16 values through this path and compares
-// each code with the CPU oracle's division. The remainder is exact only
-// while it stays normal, so blocks with s < 2^-87 (amax < 4.5e-24) or a
-// subnormal 1/s take the IEEE division instead; below that range x/s
-// rounds to a signed zero code on both paths.
+// Division: each code is E(fl32(x / s)), computed from r = RN(1/s) with
+// one exact correction step (codec.cuh).
 //
 // Waits. Every mbarrier wait gives up after PrepArgs::timeout_ns; the role
 // that gives up sets kErrTimeout in the error word and an abort flag in
 // shared memory, the others notice it and leave, and the producer first
 // waits (bounded) for its copies in flight to land.
-#include <cuda_fp8.h>
-
+#include "codec.cuh"
 #include "plan.h"
 
 namespace wt {
@@ -77,10 +61,7 @@ constexpr int kConsumerThreads = kGroups * kGroupThreads;
 constexpr int kCtaThreads = kConsumerThreads + 32;
 constexpr int kRowStride = kGroupThreads / 16;      // rows between a thread's rows
 constexpr int kRows = kTile / kRowStride;           // rows per consumer thread
-constexpr unsigned kFull = 0xFFFFFFFFu;
-// biased exponents of the scales the correction step handles: 2^-87 <= s
-// and 1/s normal
-constexpr uint32_t kMinScaleExp = 40u, kMaxScaleExp = 252u;
+
 
 struct SmemCtl {
   DevUnit meta[kStages];                 // the unit in each stage
@@ -181,33 +162,6 @@ __device__ __forceinline__ bool bar_red_or(int id, int n, bool v) {
   return r != 0;
 }
 
-__device__ __forceinline__ uint32_t ld_nc_u32(const void* p) {
-  uint32_t v;
-  asm volatile("ld.global.nc.u32 %0, [%1];" : "=r"(v) : "l"(p));
-  return v;
-}
-
-__device__ __forceinline__ uint16_t ld_nc_u16(const void* p) {
-  uint16_t v;
-  asm volatile("ld.global.nc.L1::no_allocate.u16 %0, [%1];" : "=h"(v) : "l"(p));
-  return v;
-}
-
-// max(|a|, |b|) per bf16 half; the result's sign bits are meaningless
-// (xorsign), only magnitudes are kept.
-__device__ __forceinline__ uint32_t absmax_bf16x2(uint32_t a, uint32_t b) {
-  uint32_t d;
-  asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-  return d;
-}
-
-__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
-
-// Two fp32 values -> two e4m3 codes (first value in the low byte), RNE, satfinite.
-__device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
-  return (uint32_t)__nv_cvt_float2_to_fp8x2(make_float2(lo, hi), __NV_SATFINITE, __NV_E4M3);
-}
 
 // --------------------------------------------------------- waits, abort ---
 // Wait for the phase of parity `parity`; false when it has not completed
@@ -341,13 +295,6 @@ __device__ __forceinline__ DevDstPtr load_dst(const PrepArgs& a, uint32_t i) {
   return d;
 }
 
-__device__ __forceinline__ uint4 ld_nc_v4(const void* p) {
-  uint4 v;
-  asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p));
-  return v;
-}
-
 // Where block (bi, bj) lands in one destination: the element offset of the
 // thread's first row chunk, the element step between its rows, the index
 // of the block's scale, and whether the destination holds the block at all
@@ -419,32 +366,6 @@ __device__ void gather_stage(const PrepArgs& a, const DevUnit& m, uint8_t* sp, i
       for (int c4 = 0; c4 < kTile / 32; ++c4) out[lane + 32 * c4] = e[i][c4];
     }
   }
-}
-
-// fl32(x / s) from r = RN(1/s): one correction step (see the header),
-// written with t = -e so that x = -0 gives -0 (-0 + -0), not +0.
-__device__ __forceinline__ float quotient(float x, float s, float r) {
-  const float q0 = __fmul_rn(x, r);
-  const float t = __fmaf_rn(q0, s, -x);
-  return __fmaf_rn(t, -r, q0);
-}
-
-// 8 BF16 elements (one 16-byte chunk) -> 8 codes by the correction step.
-__device__ __forceinline__ uint2 quant_chunk(const uint4& v, float s, float r) {
-  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-  uint32_t c[4];
-#pragma unroll
-  for (int k = 0; k < 4; ++k) c[k] = e4m3x2(quotient(bf16_lo(w[k]), s, r), quotient(bf16_hi(w[k]), s, r));
-  return make_uint2(__byte_perm(c[0], c[1], 0x5410), __byte_perm(c[2], c[3], 0x5410));
-}
-
-// 8 BF16 elements (one 16-byte chunk) -> 8 codes with the IEEE division.
-__device__ __forceinline__ uint2 quant_exact(const uint4& v, float s) {
-  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-  uint32_t c[4];
-#pragma unroll
-  for (int k = 0; k < 4; ++k) c[k] = e4m3x2(__fdiv_rn(bf16_lo(w[k]), s), __fdiv_rn(bf16_hi(w[k]), s));
-  return make_uint2(__byte_perm(c[0], c[1], 0x5410), __byte_perm(c[2], c[3], 0x5410));
 }
 
 // Codes of one row chunk, byte by byte (outputs whose rows are not 8-byte

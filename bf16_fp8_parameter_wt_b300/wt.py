@@ -28,7 +28,7 @@ WT_FLAG_DEBUG_CHECKS = 0x2
 EXPORTS = ["wt_plan_create", "wt_plan_pool_bytes", "wt_plan_output_layout",
            "wt_plan_shard_host_offset", "wt_plan_get_stats", "wt_prepare", "wt_prepare_offload",
            "wt_plan_check", "wt_debug_fail_offload_chunk", "wt_debug_stall_unit", "wt_plan_destroy",
-           "wt_prepare_noalloc",
+           "wt_prepare_noalloc", "wt_quantize_tokens",
            "wt_status_string", "wt_last_error"]
 
 
@@ -94,6 +94,7 @@ def lib() -> C.CDLL:
         L.wt_plan_check.argtypes = [P, P]
         L.wt_debug_fail_offload_chunk.argtypes = [P, C.c_int32]
         L.wt_debug_stall_unit.argtypes = [P, C.c_int64, C.c_uint64]
+        L.wt_quantize_tokens.argtypes = [P, C.c_int64, C.c_int64, C.c_int64, P, P, P]
         L.wt_plan_destroy.argtypes = [P]
         L.wt_status_string.restype = C.c_char_p
         L.wt_status_string.argtypes = [C.c_int]
@@ -234,6 +235,13 @@ def wt_plan_check(plan: int, stream: int = 0) -> None:
 
 def wt_debug_fail_offload_chunk(plan: int, chunk: int) -> None:
     _check(lib().wt_debug_fail_offload_chunk(plan, chunk))
+
+
+def wt_quantize_tokens(x: int, tokens: int, hidden: int, x_ld: int, codes: int, scales: int,
+                       stream: int = 0) -> None:
+    """The 1 x 128 activation codec on device buffers (see include/wt.h)."""
+    _check(lib().wt_quantize_tokens(x or None, tokens, hidden, x_ld, codes or None, scales or None,
+                                    stream or None))
 
 
 def wt_debug_stall_unit(plan: int, unit: int, wait_limit_ns: int = 0) -> None:

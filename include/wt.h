@@ -239,6 +239,23 @@ wt_status wt_prepare_offload(wt_plan* p, const void* host_image,
 wt_status wt_prepare_noalloc(const wt_plan_desc* desc, const void* const* shard_ptrs,
                              void* const* pools, void* stream);
 
+/* The activation codec of the MoE dispatch: the same e4m3 arithmetic at
+ * 1 x 128 granularity ("Enabling trillion-parameter models on AWS EFA",
+ * dispatch/combine kernels: tokens are sent as block-scaled FP8 at hidden
+ * 7168). x: tokens x hidden BF16 on the current device, row stride x_ld
+ * elements (x_ld >= hidden). For each token and each group of 128
+ * consecutive channels (the last group may be shorter): scale = amax / 448
+ * (1.0 for an all-zero group), code = e4m3_rne_satfinite(x / scale) with an
+ * IEEE binary32 quotient. codes: tokens x hidden bytes, row-major;
+ * scales: tokens x ceil(hidden / 128) fp32, row-major; both caller-owned on
+ * the same device. x 2-byte and scales 4-byte aligned; 16-byte-aligned x
+ * with hidden and x_ld multiples of 8 (and 8-byte-aligned codes) take the
+ * vector path. Asynchronous on `stream`, allocates nothing, no plan needed.
+ * Errors: WT_ERR_INVALID_ARGUMENT (hidden < 1, x_ld < hidden, NULL buffers,
+ * more than 2^31 - 1 groups), WT_ERR_ALIGNMENT, WT_ERR_CUDA. */
+wt_status wt_quantize_tokens(const void* x, int64_t tokens, int64_t hidden, int64_t x_ld,
+                             void* codes, float* scales, void* stream);
+
 /* Synchronise `stream`, then report what the kernels of earlier
  * wt_prepare* calls recorded, and clear it: WT_ERR_TIMEOUT if a wait inside
  * the kernel gave up (every wait is bounded; the step's output is then

@@ -194,3 +194,13 @@ def test_tensor_parallel_blocks_have_one_destination():
     one = llama_dense()
     norms = sum(2 * 4096 for o in one.outputs if o.name.endswith("norm"))
     assert w.bytes_written == one.bytes_written + 3 * norms
+
+
+def test_token_codec_validates_arguments_before_touching_a_device():
+    L = wt.lib()
+    assert L.wt_quantize_tokens(None, -1, 128, 128, None, None, None) == 1
+    assert L.wt_quantize_tokens(None, 4, 0, 128, None, None, None) == 1
+    assert L.wt_quantize_tokens(None, 4, 256, 128, None, None, None) == 1     # ld < hidden
+    assert L.wt_quantize_tokens(None, 4, 128, 128, None, None, None) == 1     # NULL buffers
+    assert L.wt_quantize_tokens(None, 0, 128, 128, None, None, None) == 0     # nothing to do
+    assert L.wt_quantize_tokens(2, 1 << 25, 1 << 13, 1 << 13, 16, 16, None) == 1  # > 2^31 groups
