@@ -174,13 +174,19 @@ wt_status upload(Plan& p, int device) {
 // Check the caller's pointers and, when they changed since the last call,
 // rebuild the dynamic pointer block (shard pointers, the shards' tensor
 // maps, absolute destination addresses) on the host and queue one copy on s.
-wt_status stage_pointers(Plan& p, const void* const* shards, void* const* pools, cudaStream_t s) {
+wt_status stage_pointers(Plan& p, const void* const* shards, void* const* pools, cudaStream_t s,
+                         bool capturing) {
   const size_t n_slots = (size_t)p.num_slots, n_ranks = (size_t)p.num_ranks;
   const bool shards_changed =
       shards && !(p.shards_valid && std::equal(p.cached_shards.begin(), p.cached_shards.end(), shards));
   const bool pools_changed =
       !(p.pools_valid && std::equal(p.cached_pools.begin(), p.cached_pools.end(), pools));
   if (!shards_changed && !pools_changed) return WT_OK;
+  // a captured copy would read the staging buffer at every replay, after
+  // later calls may have rewritten it
+  if (capturing)
+    return fail(WT_ERR_INVALID_ARGUMENT,
+                "new shard or pool pointers inside a stream capture: stage them with an uncaptured call first");
   if (pools_changed)
     for (size_t r = 0; r < n_ranks; ++r) {
       if (p.pool_bytes[r] == 0) continue;
@@ -325,7 +331,11 @@ wt_status wt_prepare(wt_plan* h, const void* const* shard_ptrs, void* const* poo
   DeviceGuard g(p.device);
   if (!g.ok) return fail(WT_ERR_CUDA, "cudaSetDevice failed");
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  wt_status st = stage_pointers(p, shard_ptrs, pools, s);
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  cudaError_t e = cudaStreamIsCapturing(s, &cap);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamIsCapturing");
+  const bool capturing = cap != cudaStreamCaptureStatusNone;
+  wt_status st = stage_pointers(p, shard_ptrs, pools, s, capturing);
   if (st != WT_OK) return st;
   PrepArgs a = p.args;
   a.shard_ptrs = p.d_shard_ptrs;
@@ -335,8 +345,9 @@ wt_status wt_prepare(wt_plan* h, const void* const* shard_ptrs, void* const* poo
   a.tmap_fence = p.tmaps_dirty ? 1u : 0u;
   a.unit_begin = 0;
   a.unit_end = p.num_units;
-  cudaError_t e = launch_prepare(a, grid_for(p, p.num_units), s, p.flags & WT_FLAG_DEBUG_CHECKS);
+  e = launch_prepare(a, grid_for(p, p.num_units), s, p.flags & WT_FLAG_DEBUG_CHECKS);
   if (e != cudaSuccess) return cuda_fail(e, "preparation kernel launch");
+  if (capturing) return WT_OK;         // the graph's replays are the caller's to track
   p.tmaps_dirty = false;
   if ((e = cudaEventRecord(p.last_done, s)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
   p.ran = true;
@@ -355,7 +366,11 @@ wt_status wt_prepare_offload(wt_plan* h, const void* host_image, void* const* po
   if (!g.ok) return fail(WT_ERR_CUDA, "cudaSetDevice failed");
   cudaStream_t cs = static_cast<cudaStream_t>(copy_stream);
   cudaStream_t ks = static_cast<cudaStream_t>(compute_stream);
-  wt_status st = stage_pointers(p, nullptr, pools, ks);
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(ks, &cap) != cudaSuccess || cap != cudaStreamCaptureStatusNone ||
+      cudaStreamIsCapturing(cs, &cap) != cudaSuccess || cap != cudaStreamCaptureStatusNone)
+    return fail(WT_ERR_INVALID_ARGUMENT, "wt_prepare_offload cannot be captured into a CUDA graph");
+  wt_status st = stage_pointers(p, nullptr, pools, ks, false);
   if (st != WT_OK) return st;
   PrepArgs a = p.args;
   a.shard_ptrs = p.d_offload_shard_ptrs;

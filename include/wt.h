@@ -197,6 +197,10 @@ wt_status wt_plan_get_stats(const wt_plan* p, wt_plan_stats* stats);
  * The pointer tables are re-uploaded (one stream-ordered copy) only when
  * they differ from the previous call's. Calls on one plan must be ordered
  * on one stream (the plan holds one device pointer table).
+ * CUDA graphs: a call may be captured once an uncaptured call has staged
+ * the same shard and pool pointers (a captured call with new pointers
+ * returns WT_ERR_INVALID_ARGUMENT). The plan does not track the graph's
+ * replays: finish them before destroying the plan or changing pointers.
  * Errors: WT_ERR_INVALID_ARGUMENT (null pointer where data is needed,
  * host-only plan), WT_ERR_ALIGNMENT, WT_ERR_CUDA (a launch or copy failed,
  * including an earlier asynchronous error). */
@@ -215,7 +219,7 @@ wt_status wt_prepare(wt_plan* p, const void* const* shard_ptrs,
  * untouched until then. Errors: as wt_prepare; WT_ERR_INVALID_ARGUMENT when
  * the plan was built without offload_chunk_bytes. If queueing fails midway
  * the call waits for what it queued and returns the error; the plan stays
- * usable. */
+ * usable. It cannot be captured into a CUDA graph (WT_ERR_INVALID_ARGUMENT). */
 wt_status wt_prepare_offload(wt_plan* p, const void* host_image,
                              void* const* pools, void* copy_stream,
                              void* compute_stream);

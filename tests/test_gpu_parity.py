@@ -192,6 +192,40 @@ def test_every_amax_element_pair_bit_exact(oracle_mod):
     plan.close()
 
 
+def test_captured_step_replays_from_a_cuda_graph(oracle_mod):
+    """A wt_prepare captured into a CUDA graph (after an uncaptured call has
+    staged the same pointers) writes the same bytes on every replay; new
+    pointers inside a capture are refused."""
+    w = tiny_dense()
+    shards = make_shards(w, device="cuda:0")
+    want = oracle_pools(oracle_mod, w, shards)
+    plan = wt.Plan(w, device=0)
+    pools = device_pools(plan, w.num_ranks)
+    stream = torch.cuda.Stream()
+    shard_arr, pool_arr = plan.bind([s.data_ptr() for per in shards for s in per],
+                                    [p.data_ptr() for p in pools])
+    plan.prepare(shard_arr, pool_arr, stream.cuda_stream)
+    stream.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        plan.prepare(shard_arr, pool_arr, stream.cuda_stream)
+    for _ in range(2):
+        for p in pools:
+            p.fill_(CANARY)
+        torch.cuda.synchronize()
+        graph.replay()
+        torch.cuda.synchronize()
+        assert_pools_equal(pools, want)
+    other = device_pools(plan, w.num_ranks)
+    with pytest.raises(wt.WTError) as ei:
+        with torch.cuda.graph(torch.cuda.CUDAGraph(), stream=stream):
+            other[0].add_(0)
+            plan.prepare(shard_arr, [p.data_ptr() for p in other], stream.cuda_stream)
+    assert ei.value.name == "WT_ERR_INVALID_ARGUMENT"
+    torch.cuda.synchronize()
+    plan.close()
+
+
 def test_all_zero_plan_and_misuse_errors():
     w = Workload("empty", [], [], 2)
     plan = wt.Plan(w, device=0)
