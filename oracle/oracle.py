@@ -87,6 +87,8 @@ def lib():
                                  C.c_void_p, C.c_int32]
         L.wo_quantize_tokens.argtypes = [C.c_void_p, C.c_int64, C.c_int64, C.c_int64,
                                          C.c_void_p, C.c_void_p]
+        L.wo_expected_blocks.restype = C.c_int64
+        L.wo_expected_blocks.argtypes = [C.POINTER(_Model), C.c_int32]
         _lib = L
     return _lib
 
@@ -189,6 +191,13 @@ class Model:
         if lib().wo_dst_shape(C.byref(self.c), o, d, C.byref(r), C.byref(c)):
             raise ValueError("oracle: invalid slice")
         return r.value, c.value
+
+    def expected_blocks(self, rank: int) -> int:
+        """Blocks landing at `rank` per step (its completion counter's step)."""
+        v = lib().wo_expected_blocks(C.byref(self.c), rank)
+        if v < 0:
+            raise ValueError("oracle: invalid model")
+        return int(v)
 
     def layout(self):
         """(data_off, scale_off) as lists per output of per-destination

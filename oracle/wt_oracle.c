@@ -372,6 +372,29 @@ static void copy_slice(const wo_output* out, const wo_slice* sl, int64_t rows, i
   }
 }
 
+/* READING (completion counters, the receiver-side immediate counter of the
+ * transfer engine page): one count per block landing at a destination. */
+int64_t wo_expected_blocks(const wo_model* m, int32_t rank) {
+  int64_t total = 0;
+  for (int32_t o = 0; o < m->num_outputs; ++o) {
+    const wo_output* out = &m->outputs[o];
+    int64_t r, c;
+    if (wo_output_shape(m, o, &r, &c)) return -1;
+    for (int32_t d = 0; d < out->num_dsts; ++d) {
+      if (out->dst_rank[d] != rank) continue;
+      int64_t bm = ceil_div(r, TILE), bn = ceil_div(c, TILE);
+      const wo_slice* sl = dst_slice(out, d);
+      if (sl) {
+        int64_t nb = 0;
+        for (int32_t k = 0; k < sl->num_ranges; ++k) nb += ceil_div(sl->length[k], TILE);
+        if (sl->dim == 0) bm = nb; else bn = nb;
+      }
+      total += bm * bn;
+    }
+  }
+  return total;
+}
+
 /* READING (activation codec): the dispatch kernels quantise each token's
  * hidden vector in groups of 128 channels ("block-scaled fp8 dispatch",
  * hidden 7168); the scale and code are those of the weight blocks. */

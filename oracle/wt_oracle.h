@@ -26,6 +26,8 @@
  *       offsets; slices against numpy slicing of the whole output.
  *   wo_prepare_output / wo_prepare : torch.cat of the shards (reassembly and
  *       fusion), numpy amax, exact-rational brute force on tiny tensors.
+ *   wo_expected_blocks : closed-form counts (round-robin experts, TP
+ *       partitions), sums over ranks.
  *   wo_quantize_tokens : exact-rational brute force per group, the
  *       dequantisation error bound, power-of-two scaling invariance.
  */
@@ -120,6 +122,12 @@ int wo_layout(const wo_model* m, uint64_t* data_off, uint64_t* scale_off,
 int wo_prepare_output(const wo_model* m, int32_t o,
                       const uint16_t* const* shards, uint8_t* data_out,
                       float* scale_out);
+
+/* Blocks (128 x 128 units) that rank receives per step: for every
+ * destination on that rank, the blocks of the fused tensor it holds (all
+ * of them, or the block rows / block columns of its slice). This is what a
+ * per-rank completion counter advances by in one step. */
+int64_t wo_expected_blocks(const wo_model* m, int32_t rank);
 
 /* The activation codec of the MoE dispatch (the same e4m3 arithmetic at
  * 1 x 128 granularity): x is tokens x hidden BF16 with a row stride of ld

@@ -7,7 +7,7 @@ import torch
 
 import bruteforce as bf
 from workloads import Output, Param, ValueRecipe, Workload, make_shards, shards_to_host_u16
-from workloads import edge_stress, kimi_k2_moe_layer, llama_dense, tiny_dense, tp_slices_small
+from workloads import edge_stress, kimi_k2_moe_layer, llama_dense, llama_dense_tp4, tiny_dense, tp_slices_small
 
 
 # --------------------------------------------------------------------------
@@ -331,3 +331,30 @@ def test_invalid_slices_are_rejected(oracle_mod, sl):
                  [Output("p", (0,), True, (0,), slices=(sl,))], 1)
     with pytest.raises(ValueError):
         oracle_mod.Model(w).layout()
+
+
+# --------------------------------------------------------------------------
+# completion counts per rank
+# --------------------------------------------------------------------------
+
+def test_expected_blocks_closed_forms(oracle_mod):
+    w = kimi_k2_moe_layer()
+    m = oracle_mod.Model(w)
+    per_expert = (4096 // 128) * (7168 // 128) + (7168 // 128) * (2048 // 128)   # 2688
+    assert [m.expected_blocks(r) for r in range(8)] == [49 * per_expert] + [48 * per_expert] * 7
+    tp = llama_dense_tp4()
+    mt = oracle_mod.Model(tp)
+    counts = [mt.expected_blocks(r) for r in range(4)]
+    whole = llama_dense()
+    blocks = whole.num_tiles
+    norm_blocks = sum(32 for o in whole.outputs if o.name.endswith("norm"))   # [4096, 1]: 32 x 1
+    assert sum(counts) == blocks + 3 * norm_blocks      # the norms go to all four ranks
+    # ranks differ only in their vocabulary rows of the embedding and lm_head
+    assert counts[0] == counts[1] == counts[2]
+    assert counts[0] - counts[3] == (32128 - 31872) // 128 * 32 * 2
+    ts = tp_slices_small()
+    ms = oracle_mod.Model(ts)
+    # rank 0: 'a' whole (3x3), 'a' rows 256..300 (1x3), 'a' cols [0,128)+[256,260) (3x2); 'b' rows (2x2)
+    assert ms.expected_blocks(0) == 9 + 3 + 6 + 4
+    # rank 1: 'a' rows (2x3), 'a' cols [128,260) (3x2); 'b' whole (2x2) and cols [128,136) (2x1)
+    assert ms.expected_blocks(1) == 6 + 6 + 4 + 2
