@@ -233,6 +233,8 @@ def main():
     ap.add_argument("--workload", default="kimi_k2_moe_layer",
                     choices=["kimi_k2_moe_layer", "llama_dense", "llama_dense_tp4", "edge_stress",
                              "tiny_dense", "offload_8layer", "tokens"])
+    ap.add_argument("--counters", choices=["launch", "block"], default=None,
+                    help="time the step with per-rank completion counters")
     ap.add_argument("--tokens", type=int, default=131072)
     ap.add_argument("--hidden", type=int, default=7168)
     ap.add_argument("--images", type=int, default=2)
@@ -275,6 +277,11 @@ def main():
              for r in range(w.num_ranks)]
     pool_ptrs = [p.data_ptr() for p in pools]
     shard_ptrs, pool_ptrs = plan.bind(shard_ptrs, pool_ptrs)
+    counters = None
+    if args.counters:
+        counters = torch.zeros(w.num_ranks, dtype=torch.int32, device=dev)
+        plan.set_counters(counters.data_ptr(),
+                          wt.WT_COUNT_PER_BLOCK if args.counters == "block" else wt.WT_COUNT_PER_LAUNCH)
     stream = torch.cuda.Stream(dev)
     sp = stream.cuda_stream
 
@@ -376,6 +383,7 @@ def main():
                    "parallelism": f"replicas x{world}" if world > 1 else "single"},
         "roofline": roofline, "graph_replay_us": graph_us,
         "first_step_host_ms": round(first_step_host_ms, 2), "shards": st["num_slots"],
+        "completion_counters": args.counters,
         "e2e": e2e, "cpu_baseline": cpu, "clocks": clk,
         "gpu_launches": args.steps, "wall_s_timed": round(t_wall, 4),
     }

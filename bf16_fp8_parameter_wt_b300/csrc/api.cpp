@@ -94,6 +94,16 @@ wt_status upload(Plan& p, int device) {
   const size_t o_runs = take(p.h_runs.size() * sizeof(DevRun));
   const size_t o_geom = take(p.h_geom.size() * sizeof(DevDstGeom));
   const size_t o_bmap = take(p.h_blockmap.size() * sizeof(int32_t));
+  const size_t o_drank = take(p.h_dst_rank.size() * sizeof(int32_t));
+  // per-rank block counts of a whole step and of each offload chunk
+  std::vector<uint32_t> lc((1 + p.chunks.size()) * (size_t)p.num_ranks, 0);
+  for (int32_t r = 0; r < p.num_ranks; ++r) lc[(size_t)r] = (uint32_t)p.expected_blocks[(size_t)r];
+  for (size_t c = 0; c < p.chunks.size(); ++c)
+    for (int32_t o = p.chunks[c].out_begin; o < p.chunks[c].out_end; ++o)
+      for (const DstInfo& ds : p.outputs[o].dsts)
+        lc[(1 + c) * (size_t)p.num_ranks + (size_t)ds.rank] +=
+            (uint32_t)(((ds.rows + kTile - 1) / kTile) * ((ds.cols + kTile - 1) / kTile));
+  const size_t o_lc = take(lc.size() * sizeof(uint32_t));
   const size_t o_err = take(sizeof(int32_t));
   const size_t o_offl_s = take(offload ? n_slots * sizeof(void*) : 0);
   const size_t o_offl_t = take(offload ? n_slots * kTmapBytes : 0);
@@ -108,6 +118,8 @@ wt_status upload(Plan& p, int device) {
       (e = put(o_runs, p.h_runs.data(), p.h_runs.size() * sizeof(DevRun))) != cudaSuccess ||
       (e = put(o_geom, p.h_geom.data(), p.h_geom.size() * sizeof(DevDstGeom))) != cudaSuccess ||
       (e = put(o_bmap, p.h_blockmap.data(), p.h_blockmap.size() * sizeof(int32_t))) != cudaSuccess ||
+      (e = put(o_drank, p.h_dst_rank.data(), p.h_dst_rank.size() * sizeof(int32_t))) != cudaSuccess ||
+      (e = put(o_lc, lc.data(), lc.size() * sizeof(uint32_t))) != cudaSuccess ||
       (e = cudaMemset(base + o_err, 0, sizeof(int32_t))) != cudaSuccess)
     return cuda_fail(e, "uploading plan tables");
   p.dyn_bytes = dl.bytes;
@@ -119,6 +131,8 @@ wt_status upload(Plan& p, int device) {
   p.args.runs = reinterpret_cast<const DevRun*>(base + o_runs);
   p.args.dst_ptrs = p.d_dst_ptrs;
   p.args.geom = reinterpret_cast<const DevDstGeom*>(base + o_geom);
+  p.args.dst_rank = reinterpret_cast<const int32_t*>(base + o_drank);
+  p.d_launch_counts = reinterpret_cast<uint32_t*>(base + o_lc);
   p.args.blockmap = reinterpret_cast<const int32_t*>(base + o_bmap);
   p.args.error_word = p.d_error;
   p.args.timeout_ns = kDefaultTimeoutNs;
@@ -343,10 +357,14 @@ wt_status wt_prepare(wt_plan* h, const void* const* shard_ptrs, void* const* poo
   a.stall_unit = p.stall_unit;
   a.timeout_ns = p.wait_limit_ns ? p.wait_limit_ns : kDefaultTimeoutNs;
   a.tmap_fence = p.tmaps_dirty ? 1u : 0u;
+  a.counters = p.count_mode == WT_COUNT_PER_BLOCK ? p.counters : nullptr;
   a.unit_begin = 0;
   a.unit_end = p.num_units;
   e = launch_prepare(a, grid_for(p, p.num_units), s, p.flags & WT_FLAG_DEBUG_CHECKS);
   if (e != cudaSuccess) return cuda_fail(e, "preparation kernel launch");
+  if (p.counters && p.count_mode == WT_COUNT_PER_LAUNCH &&
+      (e = launch_add_counts(p.counters, p.d_launch_counts, p.num_ranks, p.d_error, s)) != cudaSuccess)
+    return cuda_fail(e, "completion count launch");
   if (capturing) return WT_OK;         // the graph's replays are the caller's to track
   p.tmaps_dirty = false;
   if ((e = cudaEventRecord(p.last_done, s)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
@@ -375,6 +393,7 @@ wt_status wt_prepare_offload(wt_plan* h, const void* host_image, void* const* po
   PrepArgs a = p.args;
   a.shard_ptrs = p.d_offload_shard_ptrs;
   a.tmaps = p.d_offload_tmaps;
+  a.counters = p.count_mode == WT_COUNT_PER_BLOCK ? p.counters : nullptr;
   a.stall_unit = p.stall_unit;
   a.timeout_ns = p.wait_limit_ns ? p.wait_limit_ns : kDefaultTimeoutNs;
   const char* host = static_cast<const char*>(host_image);
@@ -406,6 +425,10 @@ wt_status wt_prepare_offload(wt_plan* h, const void* host_image, void* const* po
                             p.flags & WT_FLAG_DEBUG_CHECKS)) != cudaSuccess)
       return drain(WT_ERR_CUDA, std::string("preparation kernel launch: ") + cudaGetErrorString(e));
     if (c.unit_end > c.unit_begin) p.offload_tmaps_dirty = false;
+    if (p.counters && p.count_mode == WT_COUNT_PER_LAUNCH &&
+        (e = launch_add_counts(p.counters, p.d_launch_counts + (1 + i) * (size_t)p.num_ranks, p.num_ranks,
+                               p.d_error, ks)) != cudaSuccess)
+      return drain(WT_ERR_CUDA, std::string("completion count launch: ") + cudaGetErrorString(e));
     if ((e = cudaEventRecord(p.prep_done[b], ks)) != cudaSuccess)
       return drain(WT_ERR_CUDA, std::string("cudaEventRecord: ") + cudaGetErrorString(e));
     p.prep_recorded[b] = true;
@@ -437,6 +460,24 @@ wt_status wt_plan_check(wt_plan* h, void* stream) {
 wt_status wt_debug_fail_offload_chunk(wt_plan* h, int32_t chunk) {
   if (!h) return fail(WT_ERR_INVALID_ARGUMENT, "plan is NULL");
   h->p.fail_chunk = chunk;
+  return WT_OK;
+}
+
+wt_status wt_plan_set_counters(wt_plan* h, uint32_t* counters, uint32_t mode) {
+  if (!h) return fail(WT_ERR_INVALID_ARGUMENT, "plan is NULL");
+  if (h->p.device < 0 && counters) return fail(WT_ERR_INVALID_ARGUMENT, "host-only plan cannot signal");
+  if (mode != WT_COUNT_PER_LAUNCH && mode != WT_COUNT_PER_BLOCK)
+    return fail(WT_ERR_INVALID_ARGUMENT, "unknown counting mode");
+  if (reinterpret_cast<uintptr_t>(counters) % 4) return fail(WT_ERR_ALIGNMENT, "counters must be 4-byte aligned");
+  h->p.counters = counters;
+  h->p.count_mode = mode;
+  return WT_OK;
+}
+
+wt_status wt_plan_expected_count(const wt_plan* h, int32_t rank, uint64_t* count) {
+  if (!h || !count) return fail(WT_ERR_INVALID_ARGUMENT, "NULL argument");
+  if (rank < 0 || rank >= h->p.num_ranks) return fail(WT_ERR_INVALID_ARGUMENT, "rank out of range");
+  *count = h->p.expected_blocks[(size_t)rank];
   return WT_OK;
 }
 

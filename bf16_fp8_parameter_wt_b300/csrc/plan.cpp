@@ -250,6 +250,8 @@ wt_status compile_plan(const wt_plan_desc* d, Plan* p) {
   p->h_runs.clear();
   p->h_geom.clear();
   p->h_blockmap.clear();
+  p->h_dst_rank.clear();
+  p->expected_blocks.assign((size_t)p->num_ranks, 0);
   p->h_units.reserve((size_t)units);
   p->slot_rows.assign(p->num_slots, 0);
   p->slot_cols.assign(p->num_slots, 0);
@@ -269,6 +271,9 @@ wt_status compile_plan(const wt_plan_desc* d, Plan* p) {
     const int64_t tiles_m = ceil_div(oi.rows, kTile), tiles_n_all = ceil_div(oi.cols, kTile);
     bool sliced = false;
     for (const DstInfo& ds : oi.dsts) {
+      p->h_dst_rank.push_back(ds.rank);
+      p->expected_blocks[(size_t)ds.rank] +=
+          (uint64_t)(ceil_div(ds.rows, kTile) * ceil_div(ds.cols, kTile));
       DevDstGeom g;
       g.dim = ds.slice_dim;
       g.map_off = -1;

@@ -87,6 +87,8 @@ struct PrepArgs {
   const int32_t* blockmap;
   int64_t unit_begin, unit_end;
   int32_t* error_word;               // kErr* bits
+  uint32_t* counters;                // per-rank completion counters, or NULL
+  const int32_t* dst_rank;           // per destination entry: its rank
   uint64_t timeout_ns;               // limit of every wait inside the kernel
   uint32_t tmap_fence;               // tensor maps were rewritten since the last launch
   int64_t stall_unit;                // testing: this unit is never filled (-1: none)
@@ -150,6 +152,8 @@ struct Plan {
   std::vector<DevRun> h_runs;
   std::vector<DevDstGeom> h_geom;           // per destination entry
   std::vector<int32_t> h_blockmap;
+  std::vector<int32_t> h_dst_rank;          // per destination entry
+  std::vector<uint64_t> expected_blocks;    // per rank and step
   // per slot: rows and cols of the shard, and whether a tensor map is
   // encoded for it (vec outputs, non-empty shards)
   std::vector<int64_t> slot_rows, slot_cols;
@@ -186,6 +190,9 @@ struct Plan {
   cudaEvent_t prep_done[2] = {nullptr, nullptr};
   bool prep_recorded[2] = {false, false};
   int32_t fail_chunk = -1;
+  uint32_t* counters = nullptr;     // wt_plan_set_counters
+  uint32_t count_mode = 0;          // WT_COUNT_PER_LAUNCH or WT_COUNT_PER_BLOCK
+  uint32_t* d_launch_counts = nullptr;   // [1 + chunks][ranks]: a step, then each chunk
   // testing hooks (wt_debug_stall_unit)
   int64_t stall_unit = -1;
   uint64_t wait_limit_ns = 0;        // 0: kDefaultTimeoutNs
@@ -206,7 +213,14 @@ constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;   // 2 s per wait
 cudaError_t prep_kernel_setup();
 // Launch over units [a.unit_begin, a.unit_end) with grid CTAs (at most one
 // per SM is resident).
+// With a.counters set, the kernel also signals every block's completion.
 cudaError_t launch_prepare(const PrepArgs& a, int grid, cudaStream_t s, bool debug);
+
+// counters.cu: counters[i] += counts[i] for i < n, queued on s after one
+// device-scope fence (everything before it on s is complete and visible);
+// nothing is added while error_word holds kErrTimeout.
+cudaError_t launch_add_counts(uint32_t* counters, const uint32_t* counts, int32_t n, const int32_t* error_word,
+                              cudaStream_t s);
 
 }  // namespace wt
 

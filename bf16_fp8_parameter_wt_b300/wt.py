@@ -28,7 +28,8 @@ WT_FLAG_DEBUG_CHECKS = 0x2
 EXPORTS = ["wt_plan_create", "wt_plan_pool_bytes", "wt_plan_output_layout",
            "wt_plan_shard_host_offset", "wt_plan_get_stats", "wt_prepare", "wt_prepare_offload",
            "wt_plan_check", "wt_debug_fail_offload_chunk", "wt_debug_stall_unit", "wt_plan_destroy",
-           "wt_prepare_noalloc", "wt_quantize_tokens",
+           "wt_prepare_noalloc", "wt_quantize_tokens", "wt_plan_set_counters",
+           "wt_plan_expected_count", "wt_wait_counters",
            "wt_status_string", "wt_last_error"]
 
 
@@ -95,6 +96,9 @@ def lib() -> C.CDLL:
         L.wt_debug_fail_offload_chunk.argtypes = [P, C.c_int32]
         L.wt_debug_stall_unit.argtypes = [P, C.c_int64, C.c_uint64]
         L.wt_quantize_tokens.argtypes = [P, C.c_int64, C.c_int64, C.c_int64, P, P, P]
+        L.wt_plan_set_counters.argtypes = [P, P, C.c_uint32]
+        L.wt_plan_expected_count.argtypes = [P, C.c_int32, C.POINTER(C.c_uint64)]
+        L.wt_wait_counters.argtypes = [P, C.c_int32, P, C.c_uint64, P, P]
         L.wt_plan_destroy.argtypes = [P]
         L.wt_status_string.restype = C.c_char_p
         L.wt_status_string.argtypes = [C.c_int]
@@ -244,6 +248,28 @@ def wt_quantize_tokens(x: int, tokens: int, hidden: int, x_ld: int, codes: int, 
                                     stream or None))
 
 
+WT_COUNT_PER_LAUNCH = 0
+WT_COUNT_PER_BLOCK = 1
+
+
+def wt_plan_set_counters(plan: int, counters: int, mode: int = WT_COUNT_PER_LAUNCH) -> None:
+    _check(lib().wt_plan_set_counters(plan, counters or None, mode))
+
+
+def wt_plan_expected_count(plan: int, rank: int) -> int:
+    v = C.c_uint64()
+    _check(lib().wt_plan_expected_count(plan, rank, C.byref(v)))
+    return v.value
+
+
+def wt_wait_counters(counters: int, targets: Sequence[int], limit_ns: int, status: int,
+                     stream: int = 0) -> None:
+    """Queue a bounded wait until counters[i] >= targets[i] (modulo 2^32)."""
+    t = (C.c_uint32 * max(1, len(targets)))(*[int(v) & 0xFFFFFFFF for v in targets])
+    _check(lib().wt_wait_counters(counters or None, len(targets), t, limit_ns, status or None,
+                                  stream or None))
+
+
 def wt_debug_stall_unit(plan: int, unit: int, wait_limit_ns: int = 0) -> None:
     _check(lib().wt_debug_stall_unit(plan, unit, wait_limit_ns))
 
@@ -297,6 +323,12 @@ class Plan:
 
     def check(self, stream: int = 0) -> None:
         wt_plan_check(self.handle, stream)
+
+    def set_counters(self, counters: int, mode: int = WT_COUNT_PER_LAUNCH) -> None:
+        wt_plan_set_counters(self.handle, counters, mode)
+
+    def expected_count(self, rank: int) -> int:
+        return wt_plan_expected_count(self.handle, rank)
 
     def close(self) -> None:
         if self.handle:

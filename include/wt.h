@@ -273,6 +273,48 @@ wt_status wt_plan_check(wt_plan* p, void* stream);
  * drain-and-report path without touching the GPU. */
 wt_status wt_debug_fail_offload_chunk(wt_plan* p, int32_t chunk);
 
+/* Completion counters, the receiving side of the transfer stage: with
+ * counters set (a device array of num_ranks uint32, caller-owned and
+ * caller-zeroed, on the plan's device; NULL turns counting off), every
+ * later wt_prepare / wt_prepare_offload adds, for each 128 x 128 block and
+ * each destination holding it, one to counters[rank] once that block's
+ * stores to rank are visible device-wide (release at device scope). One
+ * step adds wt_plan_expected_count(rank) to each counter; a consumer that
+ * waits until counter >= base + expected (modulo 2^32) with an acquire
+ * load sees the rank's whole step. The pages' transfer engine counts the
+ * immediates of one-sided writes the same way ("RDMA point-to-point
+ * communication for LLM systems", ImmCounter).
+ *   WT_COUNT_PER_LAUNCH: the counts of each kernel launch (a whole step,
+ *     or one offload chunk, so ranks complete chunk by chunk) are added by
+ *     a small stream-ordered kernel right after it. No cost to the step.
+ *     After a launch whose waits gave up (WT_ERR_TIMEOUT), nothing is
+ *     counted until wt_plan_check has reported and cleared the error.
+ *   WT_COUNT_PER_BLOCK: blocks are counted inside the kernel as their
+ *     stores complete, in any order, so a rank can finish before the
+ *     launch does. Each count needs a device-scope release, which on B300
+ *     costs about 12 % of the step's throughput.
+ * Errors: WT_ERR_INVALID_ARGUMENT (NULL plan, host-only plan, unknown
+ * mode), WT_ERR_ALIGNMENT. */
+#define WT_COUNT_PER_LAUNCH 0u
+#define WT_COUNT_PER_BLOCK 1u
+wt_status wt_plan_set_counters(wt_plan* p, uint32_t* counters, uint32_t mode);
+
+/* Blocks that `rank` receives per step: the amount one step adds to its
+ * completion counter. */
+wt_status wt_plan_expected_count(const wt_plan* p, int32_t rank, uint64_t* count);
+
+/* A bounded device-side wait for a consumer: queues on `stream` a kernel
+ * that waits until (int32)(counters[i] - targets[i]) >= 0 for every i < n
+ * (n <= 1000; targets is a host array, copied at the call), or until
+ * limit_ns nanoseconds have passed, and then writes 0 or WT_ERR_TIMEOUT to
+ * *status (device memory). Work queued after it on `stream` sees the
+ * counted stores. It must not be the only thing that can make the
+ * counters advance on a device that cannot run both at once: queue it after
+ * the preparation on the same stream, or give it a limit. Errors:
+ * WT_ERR_INVALID_ARGUMENT, WT_ERR_ALIGNMENT, WT_ERR_CUDA. */
+wt_status wt_wait_counters(const uint32_t* counters, int32_t n, const uint32_t* targets,
+                           uint64_t limit_ns, int32_t* status, void* stream);
+
 /* Testing hook for the kernel's bounded waits: the next wt_prepare* calls
  * on this plan never fill the shared-memory stage of work unit `unit`
  * (a 128x128 block, numbered over all outputs in plan order), and every

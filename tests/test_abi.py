@@ -1,6 +1,7 @@
 """C-ABI tests that need no GPU: the library loads and exports every entry
 point include/wt.h declares; host-only plans (device -1) compile the same
 layout as the oracle; invalid descriptors return their status codes."""
+import ctypes
 import os
 import re
 
@@ -204,3 +205,31 @@ def test_token_codec_validates_arguments_before_touching_a_device():
     assert L.wt_quantize_tokens(None, 4, 128, 128, None, None, None) == 1     # NULL buffers
     assert L.wt_quantize_tokens(None, 0, 128, 128, None, None, None) == 0     # nothing to do
     assert L.wt_quantize_tokens(2, 1 << 25, 1 << 13, 1 << 13, 16, 16, None) == 1  # > 2^31 groups
+
+
+@pytest.mark.parametrize("make", [tiny_dense, llama_dense_tp4, tp_slices_small,
+                                  lambda: kimi_k2_moe_layer(12)])
+def test_expected_counts_equal_oracle(oracle_mod, make):
+    w = make()
+    m = oracle_mod.Model(w)
+    with wt.Plan(w, device=-1) as p:
+        assert [p.expected_count(r) for r in range(w.num_ranks)] == \
+               [m.expected_blocks(r) for r in range(w.num_ranks)]
+
+
+def test_counter_calls_validate_arguments():
+    L = wt.lib()
+    assert L.wt_plan_set_counters(None, None, 0) == 1
+    with wt.Plan(_simple(), device=-1) as p:
+        with pytest.raises(wt.WTError):
+            p.set_counters(256)                    # host-only plan
+        p.set_counters(0)                          # turning counting off is always fine
+        with pytest.raises(wt.WTError):
+            p.set_counters(0, 7)                   # unknown mode
+        with pytest.raises(wt.WTError):
+            p.expected_count(5)
+    t = (ctypes.c_uint32 * 1)(0)
+    assert L.wt_wait_counters(None, 1001, t, 0, None, None) == 1
+    assert L.wt_wait_counters(None, 1, t, 0, None, None) == 1
+    assert L.wt_wait_counters(16, 1, None, 0, 16, None) == 1
+    assert L.wt_wait_counters(18, 1, t, 0, 16, None) == 5         # misaligned counters
