@@ -17,7 +17,12 @@ inside the timed region. `--workload offload_8layer` instead times the
 8-layer streamed-offload stack (its own JSON line). `--impl reference` times the CPU
 oracle on the host cores on a bounded sample of the same workload.
 Under torchrun each rank prepares its own layer (weak scaling, no
-collective on the data path).
+collective on the data path). With --shard-local the ranks instead share
+one layer as an FSDP group of --fsdp ranks (default: the world size): rank
+r holds only shard r of every weight and prepares the blocks of its own
+rows with a shard-local plan, no exchange (strong scaling; `value` counts
+the bytes of all ranks). At one GPU, --shard-local --fsdp 8 times what one
+rank of an 8-way group does.
 """
 from __future__ import annotations
 
@@ -233,6 +238,9 @@ def main():
     ap.add_argument("--workload", default="kimi_k2_moe_layer",
                     choices=["kimi_k2_moe_layer", "llama_dense", "llama_dense_tp4", "edge_stress",
                              "tiny_dense", "offload_8layer", "tokens"])
+    ap.add_argument("--shard-local", action="store_true",
+                    help="FSDP group of --fsdp ranks sharing one layer; each prepares its own shard")
+    ap.add_argument("--fsdp", type=int, default=0, help="FSDP degree for --shard-local (0: world)")
     ap.add_argument("--counters", choices=["launch", "block"], default=None,
                     help="time the step with per-rank completion counters")
     ap.add_argument("--tokens", type=int, default=131072)
@@ -264,14 +272,24 @@ def main():
     wt_build.build()
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    if args.workload == "kimi_k2_moe_layer":
+    fsdp = (args.fsdp or world) if args.shard_local else 0
+    if args.shard_local:
+        if args.workload != "kimi_k2_moe_layer" or rank >= fsdp:
+            ap.error("--shard-local runs the Kimi-K2 layer with --fsdp >= the world size")
+        # one layer shared by the group: every rank draws the same values
+        w = kimi_k2_moe_layer(args.experts, shards=fsdp)
+    elif args.workload == "kimi_k2_moe_layer":
         w = kimi_k2_moe_layer(args.experts, seed=1003 + rank)
     else:
         w = WORKLOADS[args.workload]()
     shards = make_shards(w, device=dev)
+    if args.shard_local:
+        # this rank keeps its own shard of every weight and nothing else
+        shards = [[s if k == rank else s.new_empty(0) for k, s in enumerate(per)] for per in shards]
+        torch.cuda.empty_cache()
     flat = [s for per in shards for s in per]
-    shard_ptrs = [s.data_ptr() for s in flat]
-    plan = wt.Plan(w, device=local)
+    shard_ptrs = [s.data_ptr() if s.numel() else 0 for s in flat]
+    plan = wt.Plan(w, device=local, local_shard=rank if args.shard_local else -1)
     st = plan.stats
     pools = [torch.empty(max(1, plan.pool_bytes(r)), dtype=torch.uint8, device=dev)
              for r in range(w.num_ranks)]
@@ -329,7 +347,7 @@ def main():
     achieved = alg_bytes / avg_launch_s / 1e9
     traffic = (TRAFFIC["bytes_per_launch"]
                if TRAFFIC["kernel_sha256"] == kernel_sha() and args.workload == "kimi_k2_moe_layer"
-               and TRAFFIC["experts"] == args.experts else None)
+               and TRAFFIC["experts"] == args.experts and not args.shard_local else None)
     roofline = {"bound": "hbm", "achieved": round(achieved, 1),
                 "peak": peak if peak else 6400.0, "unit": "GB/s",
                 "frac": round(achieved / (peak if peak else 6400.0), 4),
@@ -357,12 +375,14 @@ def main():
         graph_us = round(g0.elapsed_time(g1) * 1e3 / 20, 2)
 
     e2e = None
-    if not args.no_e2e:
+    if args.shard_local:
+        e2e = {"value": None, "reason": "shard-local plans do not stage offloaded shards"}
+    elif not args.no_e2e:
         del pools
         torch.cuda.empty_cache()
         e2e = measure_e2e(w, shards, args, dev, world)
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and not args.shard_local:
         del shards, flat
         torch.cuda.empty_cache()
         cpu = cpu_baseline(w, args.cpu_experts)
@@ -370,7 +390,8 @@ def main():
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "higher_is_better": True, "scaling": "strong" if args.shard_local else "weak",
+        "vs_baseline": None, "dtype": "f32",
         "data": f"synthetic (seeded {w.values.dist}, sigma {w.values.sigma}, BF16, generated on device)",
         "params_per_s": round(params_per_s, 1),
         "hbm_frac_of_8TBs_spec": round(value * (alg_bytes / st["bytes_read"]) / SPEC_HBM_GBS, 4),
@@ -380,7 +401,8 @@ def main():
                    "l2": (f"inputs ({st['bytes_read'] / 1e9:.1f} GB) larger than the 126 MB L2, no flush"
                           if st["bytes_read"] > L2_BYTES else
                           "inputs smaller than L2: L2-resident, a latency figure"),
-                   "parallelism": f"replicas x{world}" if world > 1 else "single"},
+                   "parallelism": (f"shard-local rank {rank} of an FSDP group of {fsdp}" if args.shard_local
+                                   else f"replicas x{world}" if world > 1 else "single")},
         "roofline": roofline, "graph_replay_us": graph_us,
         "first_step_host_ms": round(first_step_host_ms, 2), "shards": st["num_slots"],
         "completion_counters": args.counters,

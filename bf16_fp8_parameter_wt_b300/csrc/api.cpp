@@ -213,7 +213,7 @@ wt_status stage_pointers(Plan& p, const void* const* shards, void* const* pools,
       const bool vec = p.outputs[pi.output].vec;
       for (size_t k = 0; k < pi.shard_rows.size(); ++k) {
         const void* ptr = shards[pi.slot_base + k];
-        if (pi.shard_rows[k] == 0) continue;
+        if (!p.slot_used[pi.slot_base + k]) continue;   // empty, or not this plan's shard
         if (!ptr) return fail(WT_ERR_INVALID_ARGUMENT, pi.name + ": shard " + std::to_string(k) + " is NULL");
         if (reinterpret_cast<uintptr_t>(ptr) % (vec ? 16 : 2))
           return fail(WT_ERR_ALIGNMENT, pi.name + ": shard " + std::to_string(k) + " is misaligned");

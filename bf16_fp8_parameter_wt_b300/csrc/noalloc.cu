@@ -103,7 +103,7 @@ extern "C" wt_status wt_prepare_noalloc(const wt_plan_desc* desc, const void* co
     const bool vec = p.outputs[pi.output].vec;
     for (size_t k = 0; k < pi.shard_rows.size(); ++k) {
       const void* ptr = shard_ptrs[pi.slot_base + k];
-      if (pi.shard_rows[k] == 0) continue;
+      if (!p.slot_used[pi.slot_base + k]) continue;   // empty, or not this plan's shard
       if (!ptr) return fail_na(WT_ERR_INVALID_ARGUMENT, pi.name + ": shard " + std::to_string(k) + " is NULL");
       if (reinterpret_cast<uintptr_t>(ptr) % (vec ? 16 : 2))
         return fail_na(WT_ERR_ALIGNMENT, pi.name + ": shard " + std::to_string(k) + " is misaligned");

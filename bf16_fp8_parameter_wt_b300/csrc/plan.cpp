@@ -82,8 +82,15 @@ wt_status compile_plan(const wt_plan_desc* d, Plan* p) {
     return fail(WT_ERR_INVALID_ARGUMENT, "negative count in descriptor");
   if ((d->num_params > 0 && !d->params) || (d->num_outputs > 0 && !d->outputs))
     return fail(WT_ERR_INVALID_ARGUMENT, "params/outputs array is NULL");
-  if (d->flags & ~(WT_FLAG_FORCE_NARROW | WT_FLAG_DEBUG_CHECKS))
+  if (d->flags & ~(WT_FLAG_FORCE_NARROW | WT_FLAG_DEBUG_CHECKS | WT_FLAG_SHARD_LOCAL))
     return fail(WT_ERR_INVALID_ARGUMENT, "unknown flag bits");
+  p->local_shard = -1;
+  if (d->flags & WT_FLAG_SHARD_LOCAL) {
+    if (d->local_shard < 0) return fail(WT_ERR_INVALID_ARGUMENT, "local_shard must be >= 0");
+    if (d->offload_chunk_bytes)
+      return fail(WT_ERR_INVALID_ARGUMENT, "a shard-local plan does not stage offloaded shards");
+    p->local_shard = d->local_shard;
+  }
   p->flags = d->flags;
   p->num_ranks = d->num_ranks;
 
@@ -113,7 +120,6 @@ wt_status compile_plan(const wt_plan_desc* d, Plan* p) {
     slot += pd.num_shards;
     if (slot > std::numeric_limits<int32_t>::max())
       return fail(WT_ERR_INVALID_ARGUMENT, "too many shards");
-    p->num_params_total += pd.rows * pd.cols;
   }
   p->num_slots = (int32_t)slot;
 
@@ -179,9 +185,7 @@ wt_status compile_plan(const wt_plan_desc* d, Plan* p) {
       oi.dsts[k].scale_off = soff;
       wt_status st = parse_slice(od.dst_slices ? &od.dst_slices[k] : nullptr, oi, k);
       if (st != WT_OK) return st;
-      p->bytes_written += oi.dsts[k].data_bytes + oi.dsts[k].scale_bytes;
     }
-    p->bytes_read += uint64_t(rows * cols) * 2u;
   }
   for (int i = 0; i < d->num_params; ++i)
     if (p->params[i].output < 0)
@@ -256,12 +260,18 @@ wt_status compile_plan(const wt_plan_desc* d, Plan* p) {
   p->slot_rows.assign(p->num_slots, 0);
   p->slot_cols.assign(p->num_slots, 0);
   p->slot_tmap.assign(p->num_slots, 0);
+  p->slot_used.assign(p->num_slots, 0);
   for (const auto& pi : p->params)
     for (size_t s = 0; s < pi.shard_rows.size(); ++s) {
+      // a shard-local plan reads only the shards of its own index
+      const bool used = pi.shard_rows[s] > 0 && (p->local_shard < 0 || (int64_t)s == p->local_shard);
       p->slot_rows[pi.slot_base + s] = pi.shard_rows[s];
       p->slot_cols[pi.slot_base + s] = pi.cols;
-      p->slot_tmap[pi.slot_base + s] = p->outputs[pi.output].vec && pi.shard_rows[s] > 0;
+      p->slot_used[pi.slot_base + s] = used;
+      p->slot_tmap[pi.slot_base + s] = p->outputs[pi.output].vec && used;
     }
+  p->bytes_read = p->bytes_written = 0;
+  p->num_params_total = 0;
   int32_t dst_entries = 0;
   for (int o = 0; o < (int)p->outputs.size(); ++o) {
     auto& oi = p->outputs[o];
@@ -272,8 +282,6 @@ wt_status compile_plan(const wt_plan_desc* d, Plan* p) {
     bool sliced = false;
     for (const DstInfo& ds : oi.dsts) {
       p->h_dst_rank.push_back(ds.rank);
-      p->expected_blocks[(size_t)ds.rank] +=
-          (uint64_t)(ceil_div(ds.rows, kTile) * ceil_div(ds.cols, kTile));
       DevDstGeom g;
       g.dim = ds.slice_dim;
       g.map_off = -1;
@@ -300,7 +308,7 @@ wt_status compile_plan(const wt_plan_desc* d, Plan* p) {
       auto& pi = p->params[q];
       for (size_t s = 0; s < pi.shard_rows.size(); ++s) {
         if (pi.shard_rows[s] == 0) continue;
-        p->h_runs.push_back({row, pi.shard_rows[s], pi.slot_base + (int32_t)s, 0});
+        p->h_runs.push_back({row, pi.shard_rows[s], pi.slot_base + (int32_t)s, (int32_t)s});
         row += pi.shard_rows[s];
       }
     }
@@ -308,12 +316,22 @@ wt_status compile_plan(const wt_plan_desc* d, Plan* p) {
     const uint32_t flags = (oi.format == WT_OUT_FP8_E4M3_B128 ? kUnitFp8 : 0u) |
                            (oi.vec ? kUnitVec : 0u);
     size_t k = first_run;
+    oi.unit_begin = (int64_t)p->h_units.size();
+    const uint64_t esize = oi.format == WT_OUT_FP8_E4M3_B128 ? 1u : 2u;
     for (int64_t bi = 0; bi * kTile < oi.rows; ++bi) {
       const int64_t r0 = bi * kTile;
       const int64_t nrows = std::min<int64_t>(kTile, oi.rows - r0);
       while (p->h_runs[k].row0 + p->h_runs[k].rows <= r0) ++k;
       const DevRun& run = p->h_runs[k];
       const bool single = run.row0 + run.rows >= r0 + nrows;
+      if (p->local_shard >= 0) {
+        // shard-local: this rank prepares the block rows of its own shards
+        if (!single)
+          return fail(WT_ERR_SHAPE, oi.name + ": block row " + std::to_string(bi) +
+                                        " spans shards; shard-local preparation needs shard "
+                                        "boundaries on multiples of 128 rows of every output");
+        if (run.shard != p->local_shard) continue;
+      }
       // one shard and 16-byte rows: one 2-D tensor copy from that shard
       const bool tma = single && oi.vec;
       const uint32_t f = flags | (single ? 0u : kUnitMulti) | (sliced ? kUnitSliced : 0u);
@@ -328,28 +346,34 @@ wt_status compile_plan(const wt_plan_desc* d, Plan* p) {
         u.shape = (uint32_t)(nrows - 1) | ((uint32_t)(ncols - 1) << 8) | (f << 16);
         u.num_dsts = (uint32_t)oi.dsts.size();
         u.dst_begin = (uint32_t)oi.dst_begin;
-        if (sliced) {
-          // the destinations that hold this block: when exactly one does,
-          // the unit names it alone (the kernel's single-destination path)
-          int32_t held = 0, which = -1;
-          for (size_t k = 0; k < oi.dsts.size(); ++k) {
-            const DevDstGeom& g = p->h_geom[(size_t)oi.dst_begin + k];
-            const bool in = g.dim < 0 || p->h_blockmap[(size_t)g.map_off + (size_t)(g.dim == 0 ? bi : bj)] >= 0;
-            if (in) {
-              ++held;
-              which = (int32_t)k;
-            }
-          }
-          if (held <= 1) {
-            u.num_dsts = (uint32_t)held;
-            u.dst_begin = (uint32_t)(oi.dst_begin + std::max(which, 0));
-          }
+        // the destinations that hold this block; what the step moves is
+        // counted from the units it runs
+        int32_t held = 0, which = -1;
+        const uint64_t elems = uint64_t(nrows * ncols);
+        for (size_t d = 0; d < oi.dsts.size(); ++d) {
+          const DevDstGeom& g = p->h_geom[(size_t)oi.dst_begin + d];
+          const bool in = g.dim < 0 || p->h_blockmap[(size_t)g.map_off + (size_t)(g.dim == 0 ? bi : bj)] >= 0;
+          if (!in) continue;
+          ++held;
+          which = (int32_t)d;
+          p->expected_blocks[(size_t)oi.dsts[d].rank] += 1;
+          p->bytes_written += elems * esize + (esize == 1 ? 4u : 0u);
+        }
+        p->bytes_read += elems * 2u;
+        p->num_params_total += (int64_t)elems;
+        // when exactly one destination holds it, the unit names that one
+        // alone (the kernel's single-destination path)
+        if (sliced && held <= 1) {
+          u.num_dsts = (uint32_t)held;
+          u.dst_begin = (uint32_t)(oi.dst_begin + std::max(which, 0));
         }
         p->h_units.push_back(u);
       }
     }
+    oi.num_units = (int64_t)p->h_units.size() - oi.unit_begin;
   }
   p->num_dst_entries = dst_entries;
+  p->num_units = (int64_t)p->h_units.size();
 
   // ---- packed host image for offload and its chunks ----------------------
   p->shard_host_off.assign(p->num_slots, 0);

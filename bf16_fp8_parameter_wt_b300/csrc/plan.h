@@ -50,7 +50,7 @@ struct DevRun {
   int64_t row0;            // first fused row of the run
   int64_t rows;            // number of rows
   int32_t slot;            // index into the shard pointer table
-  int32_t pad;
+  int32_t shard;           // index of that shard within its parameter
 };
 static_assert(sizeof(DevRun) == 24, "layout");
 
@@ -154,10 +154,12 @@ struct Plan {
   std::vector<int32_t> h_blockmap;
   std::vector<int32_t> h_dst_rank;          // per destination entry
   std::vector<uint64_t> expected_blocks;    // per rank and step
-  // per slot: rows and cols of the shard, and whether a tensor map is
-  // encoded for it (vec outputs, non-empty shards)
+  // per slot: rows and cols of the shard, whether the plan reads it
+  // (non-empty, and of the local index in a shard-local plan) and whether a
+  // tensor map is encoded for it (vec outputs, read shards)
   std::vector<int64_t> slot_rows, slot_cols;
-  std::vector<uint8_t> slot_tmap;
+  std::vector<uint8_t> slot_used, slot_tmap;
+  int32_t local_shard = -1;                 // >= 0: shard-local plan
 
   // device side: one allocation for the static tables, one for the
   // pointer tables that follow the caller's buffers

@@ -23,6 +23,7 @@ WT_OUT_FP8_E4M3_B128 = 1
 WT_OFFSET_AUTO = 2**64 - 1
 WT_FLAG_FORCE_NARROW = 0x1
 WT_FLAG_DEBUG_CHECKS = 0x2
+WT_FLAG_SHARD_LOCAL = 0x4
 
 # every entry point include/wt.h declares
 EXPORTS = ["wt_plan_create", "wt_plan_pool_bytes", "wt_plan_output_layout",
@@ -62,7 +63,8 @@ class wt_plan_desc(C.Structure):
     _fields_ = [("num_params", C.c_int32), ("params", C.POINTER(wt_param_desc)),
                 ("num_outputs", C.c_int32), ("outputs", C.POINTER(wt_output_desc)),
                 ("num_ranks", C.c_int32), ("pool_capacity", C.POINTER(C.c_uint64)),
-                ("offload_chunk_bytes", C.c_uint64), ("flags", C.c_uint32)]
+                ("offload_chunk_bytes", C.c_uint64), ("flags", C.c_uint32),
+                ("local_shard", C.c_int32)]
 
 
 class wt_plan_stats(C.Structure):
@@ -131,10 +133,13 @@ class PlanDesc:
     """A wt_plan_desc built from a workload-like object: .params (name,
     rows, cols, shard_rows), .outputs (name, parts, fp8, dst_ranks,
     data_off, scale_off; None offsets = automatic; slices: None or per
-    destination None / (dim, ((begin, length), ...))) and .num_ranks."""
+    destination None / (dim, ((begin, length), ...))) and .num_ranks.
+    local_shard >= 0 builds a shard-local plan (sets WT_FLAG_SHARD_LOCAL)."""
 
     def __init__(self, w, pool_capacity: Optional[Sequence[int]] = None,
-                 offload_chunk_bytes: int = 0, flags: int = 0):
+                 offload_chunk_bytes: int = 0, flags: int = 0, local_shard: int = -1):
+        if local_shard >= 0:
+            flags |= WT_FLAG_SHARD_LOCAL
         keep = []
         params = (wt_param_desc * max(1, len(w.params)))()
         for i, p in enumerate(w.params):
@@ -179,7 +184,7 @@ class PlanDesc:
             keep.append(cap)
         self._keep = (keep, params, outs)
         self.c = wt_plan_desc(len(w.params), params, len(w.outputs), outs, w.num_ranks, cap,
-                              offload_chunk_bytes, flags)
+                              offload_chunk_bytes, flags, max(local_shard, 0))
 
 
 # ---- entry points, same names as the C ABI ---------------------------------
@@ -290,8 +295,8 @@ class Plan:
     """Owning handle over a compiled plan (calls the entry points above)."""
 
     def __init__(self, w, device: int = 0, pool_capacity=None, offload_chunk_bytes: int = 0,
-                 flags: int = 0):
-        self.desc = PlanDesc(w, pool_capacity, offload_chunk_bytes, flags)
+                 flags: int = 0, local_shard: int = -1):
+        self.desc = PlanDesc(w, pool_capacity, offload_chunk_bytes, flags, local_shard)
         self.handle = wt_plan_create(self.desc, device)
         self.num_ranks = w.num_ranks
         self.num_outputs = len(w.outputs)

@@ -66,6 +66,9 @@ typedef enum {
 /* Plan flags. */
 #define WT_FLAG_FORCE_NARROW 0x1u /* use the element-wise path everywhere (testing) */
 #define WT_FLAG_DEBUG_CHECKS 0x2u /* bounds-check every store; see wt_plan_check   */
+/* Shard-local plan (FSDP rank `local_shard` prepares the blocks its own
+ * shards hold, with no exchange): see wt_plan_desc.local_shard. */
+#define WT_FLAG_SHARD_LOCAL 0x4u
 
 /* One source parameter: a rows x cols BF16 row-major tensor split along
  * dim 0 into num_shards contiguous shards of shard_rows[i] rows each
@@ -141,14 +144,27 @@ typedef struct {
   const uint64_t* pool_capacity;
   uint64_t offload_chunk_bytes;
   uint32_t flags;
+  /* With WT_FLAG_SHARD_LOCAL (ignored otherwise): the shard index this plan
+   * reads. The plan then holds only the 128-row block rows of each output
+   * that lie wholly in shard `local_shard` of their part, so that FSDP rank
+   * r, holding shard r of every param, quantizes its own rows without
+   * gathering the others' (the 128x128 scale never mixes rows of two
+   * shards). Plans for local_shard = 0 .. S-1 together write exactly what
+   * the full plan writes, each block once. Needs every shard boundary of
+   * every part on a multiple of 128 rows of its output (else
+   * WT_ERR_SHAPE); excludes offload_chunk_bytes. Layout, pool sizes and
+   * host offsets are those of the full plan; stats, expected counts and
+   * the units run are the local ones; shard pointers of other indices may
+   * be NULL. */
+  int32_t local_shard;
 } wt_plan_desc;
 
 typedef struct wt_plan wt_plan;
 
 /* Plan statistics (algorithmic sizes of one wt_prepare). */
 typedef struct {
-  int64_t num_units;          /* 128x128 tiles over all outputs              */
-  int64_t num_params_total;   /* elements of all params                       */
+  int64_t num_units;          /* 128x128 tiles this plan runs                 */
+  int64_t num_params_total;   /* elements those tiles read                    */
   uint64_t bytes_read;        /* BF16 source bytes per pass                   */
   uint64_t bytes_written;     /* destination bytes per pass (all dsts)        */
   uint64_t host_bytes;        /* size of the packed pinned image (offload)    */
@@ -187,8 +203,8 @@ wt_status wt_plan_get_stats(const wt_plan* p, wt_plan_stats* stats);
 /* One step: run the preparation of every output on `stream`.
  * shard_ptrs: num_slots device pointers, param-major then shard (the order
  *   of wt_plan_desc.params and their shard_rows); each shard is a
- *   contiguous shard_rows x cols BF16 row-major block. A shard with 0 rows
- *   may be NULL. Shards of outputs whose cols are a multiple of 8 must be
+ *   contiguous shard_rows x cols BF16 row-major block. A shard with 0 rows,
+ *   or one that a shard-local plan does not read, may be NULL. Shards of outputs whose cols are a multiple of 8 must be
  *   16-byte aligned.
  * pools: num_ranks device pointers, each 16-byte aligned, holding at least
  *   wt_plan_pool_bytes bytes (NULL allowed for a 0-byte pool).

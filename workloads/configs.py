@@ -299,12 +299,14 @@ def _moe_experts(b: _Builder, prefix: str, experts: int, hidden: int, inter: int
         b.output(f"{prefix}e{e}.down", [w2], True, (rank,))
 
 
-def kimi_k2_moe_layer(experts: int = 385, seed: int = 1003) -> Workload:
+def kimi_k2_moe_layer(experts: int = 385, seed: int = 1003, shards: int = 8) -> Workload:
     """One Kimi-K2-shaped MoE layer: 384 routed experts plus the shared one
     (index 384), each w1/w3 2048x7168 fused into gate_up 4096x7168 and w2
     7168x2048, 8 dim-0 shards per weight, expert e on rank e % 8, all FP8,
-    N(0, 0.006). `experts` < 385 gives the first `experts` of them."""
-    b = _Builder(f"kimi_k2_moe_layer_e{experts}", 8, 8, ValueRecipe("normal", 0.006, seed))
+    N(0, 0.006). `experts` < 385 gives the first `experts` of them;
+    `shards` changes the FSDP degree (the values do not depend on it)."""
+    name = f"kimi_k2_moe_layer_e{experts}" + ("" if shards == 8 else f"_s{shards}")
+    b = _Builder(name, 8, shards, ValueRecipe("normal", 0.006, seed))
     _moe_experts(b, "", experts, 7168, 2048)
     return b.w
 
@@ -321,6 +323,34 @@ def edge_stress() -> Workload:
     b.output("A", [b.param("A", 7168, 2050)], True, (0,))
     b.output("B", [b.param("B", 1000, 7168)], True, (1,))
     b.output("C_embed", [b.param("C_embed", 163840, 7168)], False, (2,))
+    return b.w
+
+
+def shard_local_mix(shards: int = 4) -> Workload:
+    """Cases for shard-local preparation, where every FSDP shard boundary
+    falls on a multiple of 128 rows of its output: empty shards, a ragged
+    last block row, a fused qkv whose parts live on different shards,
+    narrow (cols % 8 != 0) and 16-byte rows, a ragged last column block,
+    FP8 and BF16, dim-1 tensor-parallel slices, a replicated output and a
+    1-column norm; 4 shards (2: neighbouring pairs merged), 3 ranks.
+    Student-t(3) x 0.02 values, one block in eight all-zero and one in
+    eight with a +-3e4 outlier, seed 1007."""
+    splits = {"A": (384, 0, 512, 104), "B": (128, 128, 0, 264), "q": (256, 256, 0, 0),
+              "k": (0, 0, 128, 0), "v": (0, 0, 0, 128), "emb": (128, 256, 256, 0),
+              "norm": (256, 44, 0, 0)}
+    if shards == 2:
+        splits = {k: (v[0] + v[1], v[2] + v[3]) for k, v in splits.items()}
+    elif shards != 4:
+        raise ValueError("shard_local_mix has 4 or 2 shards")
+    vals = ValueRecipe("student_t3", 0.02, 1007, zero_tile_eighths=1,
+                       outlier_tile_eighths=1, outlier=3.0e4)
+    b = _Builder(f"shard_local_mix_s{shards}", 3, shards, vals)
+    b.output("A", [b.param("A", 1000, 2050, splits["A"])], True, (0,))
+    b.output("B", [b.param("B", 520, 1040, splits["B"])], True, (0, 2))
+    qkv = [b.param(n, r, 1024, splits[n]) for n, r in (("q", 512), ("k", 128), ("v", 128))]
+    b.output("qkv", qkv, True, (1, 2), slices=((1, ((0, 512),)), (1, ((512, 512),))))
+    b.output("emb", [b.param("emb", 640, 132, splits["emb"])], False, (2,))
+    b.output("norm", [b.param("norm", 300, 1, splits["norm"])], False, (0, 1))
     return b.w
 
 
@@ -343,6 +373,7 @@ WORKLOADS = {
     "llama_dense": llama_dense,
     "llama_dense_tp4": llama_dense_tp4,
     "tp_slices_small": tp_slices_small,
+    "shard_local_mix": shard_local_mix,
     "kimi_k2_moe_layer": kimi_k2_moe_layer,
     "edge_stress": edge_stress,
     "offload_layer": offload_layer,
