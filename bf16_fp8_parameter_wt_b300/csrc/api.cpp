@@ -324,6 +324,15 @@ wt_status wt_plan_shard_host_offset(const wt_plan* h, int32_t param, int32_t sha
   return WT_OK;
 }
 
+wt_status wt_plan_shard_rows_read(const wt_plan* h, int32_t param, int32_t shard, int64_t* rows) {
+  if (!h || !rows) return fail(WT_ERR_INVALID_ARGUMENT, "NULL argument");
+  if (param < 0 || param >= (int32_t)h->p.params.size()) return fail(WT_ERR_INVALID_ARGUMENT, "param out of range");
+  const ParamInfo& pi = h->p.params[param];
+  if (shard < 0 || shard >= (int32_t)pi.shard_rows.size()) return fail(WT_ERR_INVALID_ARGUMENT, "shard out of range");
+  *rows = h->p.slot_read_rows[pi.slot_base + shard];
+  return WT_OK;
+}
+
 wt_status wt_plan_get_stats(const wt_plan* h, wt_plan_stats* st) {
   if (!h || !st) return fail(WT_ERR_INVALID_ARGUMENT, "NULL argument");
   st->num_units = h->p.num_units;

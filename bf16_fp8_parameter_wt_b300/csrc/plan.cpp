@@ -82,8 +82,10 @@ wt_status compile_plan(const wt_plan_desc* d, Plan* p) {
     return fail(WT_ERR_INVALID_ARGUMENT, "negative count in descriptor");
   if ((d->num_params > 0 && !d->params) || (d->num_outputs > 0 && !d->outputs))
     return fail(WT_ERR_INVALID_ARGUMENT, "params/outputs array is NULL");
-  if (d->flags & ~(WT_FLAG_FORCE_NARROW | WT_FLAG_DEBUG_CHECKS | WT_FLAG_SHARD_LOCAL))
+  if (d->flags & ~(WT_FLAG_FORCE_NARROW | WT_FLAG_DEBUG_CHECKS | WT_FLAG_SHARD_LOCAL | WT_FLAG_SHARD_HALO))
     return fail(WT_ERR_INVALID_ARGUMENT, "unknown flag bits");
+  if ((d->flags & WT_FLAG_SHARD_HALO) && !(d->flags & WT_FLAG_SHARD_LOCAL))
+    return fail(WT_ERR_INVALID_ARGUMENT, "WT_FLAG_SHARD_HALO needs WT_FLAG_SHARD_LOCAL");
   p->local_shard = -1;
   if (d->flags & WT_FLAG_SHARD_LOCAL) {
     if (d->local_shard < 0) return fail(WT_ERR_INVALID_ARGUMENT, "local_shard must be >= 0");
@@ -261,15 +263,20 @@ wt_status compile_plan(const wt_plan_desc* d, Plan* p) {
   p->slot_cols.assign(p->num_slots, 0);
   p->slot_tmap.assign(p->num_slots, 0);
   p->slot_used.assign(p->num_slots, 0);
+  p->slot_read_rows.assign(p->num_slots, 0);
   for (const auto& pi : p->params)
     for (size_t s = 0; s < pi.shard_rows.size(); ++s) {
-      // a shard-local plan reads only the shards of its own index
-      const bool used = pi.shard_rows[s] > 0 && (p->local_shard < 0 || (int64_t)s == p->local_shard);
+      // a shard-local plan reads the shards of its own index whole (and,
+      // with halos, leading rows of others: found below)
+      const bool own = p->local_shard < 0 || (int64_t)s == p->local_shard;
       p->slot_rows[pi.slot_base + s] = pi.shard_rows[s];
       p->slot_cols[pi.slot_base + s] = pi.cols;
-      p->slot_used[pi.slot_base + s] = used;
-      p->slot_tmap[pi.slot_base + s] = p->outputs[pi.output].vec && used;
+      p->slot_read_rows[pi.slot_base + s] = own ? pi.shard_rows[s] : 0;
+      // tensor maps only for whole shards: a one-shard block lies in a shard
+      // of this plan's own index
+      p->slot_tmap[pi.slot_base + s] = p->outputs[pi.output].vec && own && pi.shard_rows[s] > 0;
     }
+  const bool halo = (p->flags & WT_FLAG_SHARD_HALO) != 0;
   p->bytes_read = p->bytes_written = 0;
   p->num_params_total = 0;
   int32_t dst_entries = 0;
@@ -325,12 +332,20 @@ wt_status compile_plan(const wt_plan_desc* d, Plan* p) {
       const DevRun& run = p->h_runs[k];
       const bool single = run.row0 + run.rows >= r0 + nrows;
       if (p->local_shard >= 0) {
-        // shard-local: this rank prepares the block rows of its own shards
-        if (!single)
+        // shard-local: a block row belongs to the shard holding its first
+        // row; without halos it must lie wholly in that shard
+        if (!single && !halo)
           return fail(WT_ERR_SHAPE, oi.name + ": block row " + std::to_string(bi) +
                                         " spans shards; shard-local preparation needs shard "
-                                        "boundaries on multiples of 128 rows of every output");
+                                        "boundaries on multiples of 128 rows of every output "
+                                        "(or WT_FLAG_SHARD_HALO)");
         if (run.shard != p->local_shard) continue;
+        // the leading rows of later shards that this block reads (its halo)
+        for (size_t q = k + 1; q < p->h_runs.size() && p->h_runs[q].row0 < r0 + nrows; ++q) {
+          const DevRun& hr = p->h_runs[q];
+          int64_t& got = p->slot_read_rows[(size_t)hr.slot];
+          got = std::max(got, std::min(hr.rows, r0 + nrows - hr.row0));
+        }
       }
       // one shard and 16-byte rows: one 2-D tensor copy from that shard
       const bool tma = single && oi.vec;
@@ -374,6 +389,7 @@ wt_status compile_plan(const wt_plan_desc* d, Plan* p) {
   }
   p->num_dst_entries = dst_entries;
   p->num_units = (int64_t)p->h_units.size();
+  for (int32_t s = 0; s < p->num_slots; ++s) p->slot_used[(size_t)s] = p->slot_read_rows[(size_t)s] > 0;
 
   // ---- packed host image for offload and its chunks ----------------------
   p->shard_host_off.assign(p->num_slots, 0);

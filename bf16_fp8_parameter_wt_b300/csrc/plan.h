@@ -158,6 +158,7 @@ struct Plan {
   // (non-empty, and of the local index in a shard-local plan) and whether a
   // tensor map is encoded for it (vec outputs, read shards)
   std::vector<int64_t> slot_rows, slot_cols;
+  std::vector<int64_t> slot_read_rows;      // leading rows of the shard read
   std::vector<uint8_t> slot_used, slot_tmap;
   int32_t local_shard = -1;                 // >= 0: shard-local plan
 

@@ -11,6 +11,16 @@ data path beyond the full_tensor() gather itself.
 assign_sources() is that choice: a deterministic greedy balance of the
 outputs' bytes (read + written) over `world` sources, largest first, ties
 to the lower rank. rank_view() is the sub-workload one source prepares.
+
+The other partition keeps FSDP's own placement: rank r of a group holds
+shard r of every parameter and prepares, with a shard-local plan, the
+128-row block rows that start in its shard. Where a shard boundary is off
+the 128-row grid, the block row that spans it also needs the leading rows
+of the next shard(s) -- at most 127 rows per boundary instead of the
+whole parameter that full_tensor() gathers. halo_transfers() lists those
+row runs for the whole group (from the plans' own wt_plan_shard_rows_read
+answers) and exchange_halos() moves them with point-to-point sends over a
+torch.distributed group.
 """
 from __future__ import annotations
 
@@ -44,3 +54,49 @@ def rank_view(w, world: int, rank: int):
     src = assign_sources(w, world)
     mine = [o for o in range(len(w.outputs)) if src[o] == rank]
     return w.subset(mine, name=f"{w.name}[source {rank}/{world}]"), mine
+
+
+def halo_transfers(w, fsdp: int) -> List[tuple]:
+    """(src rank, dst rank, param, shard, rows) for every halo the
+    shard-local plans of an FSDP group of `fsdp` ranks read: rank dst needs
+    the first `rows` rows of shard `shard` of param `param`, held by rank
+    src == shard. Host-only plans; the same list on every rank."""
+    from . import wt
+    out = []
+    for r in range(fsdp):
+        with wt.Plan(w, device=-1, local_shard=r, halo=True) as p:
+            for i, par in enumerate(w.params):
+                for k in range(len(par.shard_rows)):
+                    if k == r:
+                        continue
+                    n = p.shard_rows_read(i, k)
+                    if n:
+                        if k >= fsdp:
+                            raise ValueError(f"{par.name}: shard {k} has no rank in a group of {fsdp}")
+                        out.append((k, r, i, k, n))
+    return out
+
+
+def exchange_halos(w, transfers, rank: int, own_shards, group=None) -> dict:
+    """Send the leading rows of this rank's shards that other ranks need and
+    receive this rank's halos. own_shards[p] is this rank's shard of param p
+    (a [shard_rows, cols] BF16 tensor on the group's device). Returns
+    {(param, shard): [rows, cols] tensor} of the received halo rows."""
+    import torch
+    import torch.distributed as dist
+    reqs, keep, got = [], [], {}
+    dev = next((t.device for t in own_shards if t is not None), torch.device("cpu"))
+    # raw 16-bit payloads (no reduction happens, so the dtype is only a
+    # size); one tag per transfer so that messages pair up unambiguously
+    for tag, (src, dst, p, k, n) in enumerate(transfers):
+        if src == rank and dst != rank:
+            t = own_shards[p][:n].contiguous().view(torch.int16)
+            keep.append(t)
+            reqs.append(dist.isend(t, dst, group=group, tag=tag))
+        elif dst == rank and src != rank:
+            buf = torch.empty((n, w.params[p].cols), dtype=torch.int16, device=dev)
+            got[(p, k)] = buf.view(torch.bfloat16)
+            reqs.append(dist.irecv(buf, src, group=group, tag=tag))
+    for q in reqs:
+        q.wait()
+    return got

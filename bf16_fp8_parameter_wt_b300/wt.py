@@ -24,10 +24,11 @@ WT_OFFSET_AUTO = 2**64 - 1
 WT_FLAG_FORCE_NARROW = 0x1
 WT_FLAG_DEBUG_CHECKS = 0x2
 WT_FLAG_SHARD_LOCAL = 0x4
+WT_FLAG_SHARD_HALO = 0x8
 
 # every entry point include/wt.h declares
 EXPORTS = ["wt_plan_create", "wt_plan_pool_bytes", "wt_plan_output_layout",
-           "wt_plan_shard_host_offset", "wt_plan_get_stats", "wt_prepare", "wt_prepare_offload",
+           "wt_plan_shard_host_offset", "wt_plan_shard_rows_read", "wt_plan_get_stats", "wt_prepare", "wt_prepare_offload",
            "wt_plan_check", "wt_debug_fail_offload_chunk", "wt_debug_stall_unit", "wt_plan_destroy",
            "wt_prepare_noalloc", "wt_quantize_tokens", "wt_plan_set_counters",
            "wt_plan_expected_count", "wt_wait_counters",
@@ -90,6 +91,7 @@ def lib() -> C.CDLL:
         L.wt_plan_output_layout.argtypes = [P, C.c_int32, C.c_int32, C.POINTER(C.c_int32),
                                             C.POINTER(C.c_uint64), C.POINTER(C.c_uint64)]
         L.wt_plan_shard_host_offset.argtypes = [P, C.c_int32, C.c_int32, C.POINTER(C.c_uint64)]
+        L.wt_plan_shard_rows_read.argtypes = [P, C.c_int32, C.c_int32, C.POINTER(C.c_int64)]
         L.wt_plan_get_stats.argtypes = [P, C.POINTER(wt_plan_stats)]
         L.wt_prepare.argtypes = [P, P, P, P]
         L.wt_prepare_offload.argtypes = [P, P, P, P, P]
@@ -134,12 +136,14 @@ class PlanDesc:
     rows, cols, shard_rows), .outputs (name, parts, fp8, dst_ranks,
     data_off, scale_off; None offsets = automatic; slices: None or per
     destination None / (dim, ((begin, length), ...))) and .num_ranks.
-    local_shard >= 0 builds a shard-local plan (sets WT_FLAG_SHARD_LOCAL)."""
+    local_shard >= 0 builds a shard-local plan (sets WT_FLAG_SHARD_LOCAL;
+    halo=True also sets WT_FLAG_SHARD_HALO)."""
 
     def __init__(self, w, pool_capacity: Optional[Sequence[int]] = None,
-                 offload_chunk_bytes: int = 0, flags: int = 0, local_shard: int = -1):
+                 offload_chunk_bytes: int = 0, flags: int = 0, local_shard: int = -1,
+                 halo: bool = False):
         if local_shard >= 0:
-            flags |= WT_FLAG_SHARD_LOCAL
+            flags |= WT_FLAG_SHARD_LOCAL | (WT_FLAG_SHARD_HALO if halo else 0)
         keep = []
         params = (wt_param_desc * max(1, len(w.params)))()
         for i, p in enumerate(w.params):
@@ -205,6 +209,12 @@ def wt_plan_output_layout(plan: int, out: int, dst: int):
     r, d, s = C.c_int32(), C.c_uint64(), C.c_uint64()
     _check(lib().wt_plan_output_layout(plan, out, dst, C.byref(r), C.byref(d), C.byref(s)))
     return r.value, d.value, s.value
+
+
+def wt_plan_shard_rows_read(plan: int, param: int, shard: int) -> int:
+    v = C.c_int64()
+    _check(lib().wt_plan_shard_rows_read(plan, param, shard, C.byref(v)))
+    return v.value
 
 
 def wt_plan_shard_host_offset(plan: int, param: int, shard: int) -> int:
@@ -295,8 +305,8 @@ class Plan:
     """Owning handle over a compiled plan (calls the entry points above)."""
 
     def __init__(self, w, device: int = 0, pool_capacity=None, offload_chunk_bytes: int = 0,
-                 flags: int = 0, local_shard: int = -1):
-        self.desc = PlanDesc(w, pool_capacity, offload_chunk_bytes, flags, local_shard)
+                 flags: int = 0, local_shard: int = -1, halo: bool = False):
+        self.desc = PlanDesc(w, pool_capacity, offload_chunk_bytes, flags, local_shard, halo)
         self.handle = wt_plan_create(self.desc, device)
         self.num_ranks = w.num_ranks
         self.num_outputs = len(w.outputs)
@@ -306,6 +316,9 @@ class Plan:
 
     def output_layout(self, out: int, dst: int):
         return wt_plan_output_layout(self.handle, out, dst)
+
+    def shard_rows_read(self, param: int, shard: int) -> int:
+        return wt_plan_shard_rows_read(self.handle, param, shard)
 
     def shard_host_offset(self, param: int, shard: int) -> int:
         return wt_plan_shard_host_offset(self.handle, param, shard)

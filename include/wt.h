@@ -69,6 +69,12 @@ typedef enum {
 /* Shard-local plan (FSDP rank `local_shard` prepares the blocks its own
  * shards hold, with no exchange): see wt_plan_desc.local_shard. */
 #define WT_FLAG_SHARD_LOCAL 0x4u
+/* With WT_FLAG_SHARD_LOCAL: shard boundaries may lie off the 128-row grid.
+ * A block row then belongs to the shard holding its first row, and the
+ * rank also reads the leading rows of the following shards that the block
+ * spans (its halo, at most 127 rows per boundary, never a whole gather);
+ * wt_plan_shard_rows_read says how many rows of each shard. */
+#define WT_FLAG_SHARD_HALO 0x8u
 
 /* One source parameter: a rows x cols BF16 row-major tensor split along
  * dim 0 into num_shards contiguous shards of shard_rows[i] rows each
@@ -152,10 +158,12 @@ typedef struct {
    * shards). Plans for local_shard = 0 .. S-1 together write exactly what
    * the full plan writes, each block once. Needs every shard boundary of
    * every part on a multiple of 128 rows of its output (else
-   * WT_ERR_SHAPE); excludes offload_chunk_bytes. Layout, pool sizes and
+   * WT_ERR_SHAPE) unless WT_FLAG_SHARD_HALO is set, in which case a block
+   * row belongs to the shard of its first row and the plan reads halo rows
+   * of the next shards; excludes offload_chunk_bytes. Layout, pool sizes and
    * host offsets are those of the full plan; stats, expected counts and
    * the units run are the local ones; shard pointers of other indices may
-   * be NULL. */
+   * be NULL (see wt_plan_shard_rows_read). */
   int32_t local_shard;
 } wt_plan_desc;
 
@@ -198,13 +206,24 @@ wt_status wt_plan_output_layout(const wt_plan* p, int32_t out, int32_t dst,
 wt_status wt_plan_shard_host_offset(const wt_plan* p, int32_t param,
                                     int32_t shard, uint64_t* off);
 
+/* How many leading rows of (param, shard) one step of this plan reads:
+ * every row for a full plan; for a shard-local plan, every row of the
+ * shards of its own index, the halo rows of the shards its blocks span
+ * into (WT_FLAG_SHARD_HALO), 0 otherwise. A shard with 0 rows read may be
+ * NULL in wt_prepare; one with r < shard_rows rows read needs only its
+ * first r rows valid at the pointer passed (a halo buffer received from
+ * the rank that holds the shard). */
+wt_status wt_plan_shard_rows_read(const wt_plan* p, int32_t param, int32_t shard,
+                                  int64_t* rows);
+
 wt_status wt_plan_get_stats(const wt_plan* p, wt_plan_stats* stats);
 
 /* One step: run the preparation of every output on `stream`.
  * shard_ptrs: num_slots device pointers, param-major then shard (the order
  *   of wt_plan_desc.params and their shard_rows); each shard is a
  *   contiguous shard_rows x cols BF16 row-major block. A shard with 0 rows,
- *   or one that a shard-local plan does not read, may be NULL. Shards of outputs whose cols are a multiple of 8 must be
+ *   or one that a shard-local plan does not read, may be NULL; of a halo
+ *   shard only the rows read need be valid (wt_plan_shard_rows_read). Shards of outputs whose cols are a multiple of 8 must be
  *   16-byte aligned.
  * pools: num_ranks device pointers, each 16-byte aligned, holding at least
  *   wt_plan_pool_bytes bytes (NULL allowed for a 0-byte pool).

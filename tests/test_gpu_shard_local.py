@@ -14,13 +14,19 @@ its own dim-0 shard, no exchange).
   completion counters then read the full plan's expected counts.
 - At the full Kimi-K2 layer size the union of the 8 local plans is
   byte-identical to the full plan's output.
+- Halo plans (shard boundaries off the 128-row grid): the same checks,
+  with each halo slot pointing at a copy of the shard whose rows past the
+  reported halo are negated (a read past the halo changes the result),
+  then with halo buffers holding exactly the rows reported and NULL for
+  every other shard; on the Llama stack the 8 halo plans together (with
+  decoys past the halos) equal the full plan.
 """
 import pytest
 import torch
 
 import bf16_fp8_parameter_wt_b300 as wt
 from gpu_helpers import CANARY, assert_pools_equal, device_pools, oracle_pools
-from workloads import kimi_k2_moe_layer, make_shards, shard_local_mix
+from workloads import halo_mix, kimi_k2_moe_layer, llama_dense, make_shards, shard_local_mix
 
 pytestmark = pytest.mark.gpu
 
@@ -124,5 +130,82 @@ def test_kimi_k2_layer_full_size_union_equals_full_plan():
             total += plan.stats["bytes_read"]
             _run(plan, _ptrs(src, s, None), pools)
     assert total == w.bytes_read
+    for r in range(w.num_ranks):
+        assert torch.equal(pools[r], ref[r]), f"rank {r}"
+
+
+def _halo_ptrs(w, plan, src, s, exact, keep):
+    """Pointers for halo plan s: its own shards, halo buffers (a copy of the
+    shard with the rows past the halo negated, or exactly the halo rows),
+    and for the rest the negated shard (exact=False) or NULL."""
+    out = []
+    for i, per in enumerate(src):
+        for k, x in enumerate(per):
+            n = plan.shard_rows_read(i, k)
+            if k == s or not x.numel():
+                out.append(x.data_ptr() if x.numel() else 0)
+            elif n and exact:
+                t = x[:n].clone()
+                keep.append(t)
+                out.append(t.data_ptr())
+            elif n:
+                t = x.clone()
+                t[n:] = -t[n:]
+                keep.append(t)
+                out.append(t.data_ptr())
+            elif exact:
+                out.append(0)
+            else:
+                t = -x
+                keep.append(t)
+                out.append(t.data_ptr())
+    return out
+
+
+@pytest.mark.parametrize("shards", [4, 2])
+def test_halo_plans_write_their_own_blocks_from_own_and_halo_rows(oracle_mod, shards):
+    w = halo_mix(shards)
+    src = make_shards(w, device="cuda:0")
+    want = [torch.from_numpy(x).to("cuda:0") for x in oracle_pools(oracle_mod, w, src)]
+    with wt.Plan(w, device=0) as full:
+        _, full_mask = _written(full, _all(src), w.num_ranks)
+    union = [torch.zeros_like(m) for m in full_mask]
+    for s in range(shards):
+        with wt.Plan(w, device=0, local_shard=s, halo=True) as plan:
+            keep = []
+            got, mask = _written(plan, _halo_ptrs(w, plan, src, s, False, keep), w.num_ranks)
+            n = 0
+            for r in range(w.num_ranks):
+                k = want[r].numel()
+                m = mask[r][:k]
+                assert not bool(mask[r][k:].any()), f"shard {s}: write past pool {r}"
+                assert torch.equal(got[r][:k][m], want[r][m]), f"shard {s}, rank {r}"
+                assert not bool((union[r][:k] & m).any()), f"shard {s} rewrote another's bytes"
+                union[r][:k] |= m
+                n += int(m.sum())
+            assert n == plan.stats["bytes_written"]
+    for r in range(w.num_ranks):
+        assert torch.equal(union[r], full_mask[r]), f"rank {r}: union differs from the full plan"
+    # exactly-sized halo buffers and NULL for every shard a plan does not read
+    with wt.Plan(w, device=0) as full:
+        pools = device_pools(full, w.num_ranks)
+    for s in range(shards):
+        with wt.Plan(w, device=0, local_shard=s, halo=True) as plan:
+            keep = []
+            _run(plan, _halo_ptrs(w, plan, src, s, True, keep), pools)
+    assert_pools_equal(pools, [x.cpu().numpy() for x in want])
+
+
+def test_llama_halo_plans_together_equal_the_full_plan():
+    w = llama_dense()
+    src = make_shards(w, device="cuda:0")
+    with wt.Plan(w, device=0) as full:
+        ref = device_pools(full, w.num_ranks)
+        _run(full, _all(src), ref)
+    pools = [torch.full_like(p, CANARY) for p in ref]
+    for s in range(8):
+        with wt.Plan(w, device=0, local_shard=s, halo=True) as plan:
+            keep = []                               # full-size buffers, decoys past the halo
+            _run(plan, _halo_ptrs(w, plan, src, s, False, keep), pools)
     for r in range(w.num_ranks):
         assert torch.equal(pools[r], ref[r]), f"rank {r}"

@@ -17,6 +17,12 @@ full_tensor() gather is what the shortcut avoids).
 - Two gloo ranks each compile their own local plan and run the oracle on
   their own shards only; rank 0 checks the union against the full oracle.
 - Misaligned shards, offload and bad arguments are refused.
+- With halos (WT_FLAG_SHARD_HALO) boundaries may be off the grid: a block
+  row belongs to the shard holding its first row, and the plan reports,
+  per shard, the leading rows it reads; those match a count made here,
+  the local plans still partition the full plan, and two gloo ranks that
+  exchange exactly those rows (schedule.exchange_halos) and run the
+  oracle on what they hold reproduce the full oracle output.
 """
 import ctypes
 import hashlib
@@ -29,7 +35,8 @@ import torch.distributed as dist
 import torch.multiprocessing as mp
 
 import bf16_fp8_parameter_wt_b300 as wt
-from workloads import (TILE, Output, Param, Workload, kimi_k2_moe_layer, llama_dense,
+from bf16_fp8_parameter_wt_b300.schedule import exchange_halos, halo_transfers
+from workloads import (TILE, Output, Param, Workload, halo_mix, kimi_k2_moe_layer, llama_dense,
                        make_shards, shard_local_mix, shards_to_host_u16, tiny_dense)
 
 
@@ -51,9 +58,40 @@ def shard_runs(w, o, s):
     return out
 
 
-def owned_block_rows(w, o, s):
-    """Block rows of output o whose rows all come from shard s."""
+def owned_block_rows(w, o, s, halo=False):
+    """Block rows of output o whose rows all come from shard s (halo: whose
+    first row does)."""
+    if halo:
+        # the multiples of 128 that fall inside one of shard s's runs
+        return sorted(start // TILE for (r0, n, _) in shard_runs(w, o, s)
+                      for start in range(_cdiv(r0, TILE) * TILE, r0 + n, TILE))
     return [b for (r0, n, _) in shard_runs(w, o, s) for b in range(r0 // TILE, _cdiv(r0 + n, TILE))]
+
+
+def all_runs(w, o):
+    """(fused row begin, rows, param, shard) of every non-empty shard of output o."""
+    out, row = [], 0
+    for p in w.outputs[o].parts:
+        for k, n in enumerate(w.params[p].shard_rows):
+            if n:
+                out.append((row, n, p, k))
+            row += n
+    return out
+
+
+def halo_rows_needed(w, s):
+    """{(param, shard): leading rows} that shard s's halo plan reads from
+    shards of other indices."""
+    need = {}
+    for o in range(len(w.outputs)):
+        m, _ = w.output_shape(o)
+        for bi in owned_block_rows(w, o, s, halo=True):
+            lo, hi = bi * TILE, min(m, bi * TILE + TILE)
+            for r0, n, p, k in all_runs(w, o):
+                if k != s and r0 < hi and r0 + n > lo:
+                    assert r0 > lo                     # a halo is always a prefix
+                    need[(p, k)] = max(need.get((p, k), 0), min(n, hi - r0))
+    return need
 
 
 def held_blocks(w, o, d, block_rows):
@@ -74,13 +112,13 @@ def held_blocks(w, o, d, block_rows):
     return held
 
 
-def local_counts(w, s):
+def local_counts(w, s, halo=False):
     """Units, elements, bytes written and per-rank blocks of shard s's work."""
     units = elems = written = 0
     per_rank = [0] * w.num_ranks
     for o, out in enumerate(w.outputs):
         m, n = w.output_shape(o)
-        rows = owned_block_rows(w, o, s)
+        rows = owned_block_rows(w, o, s, halo)
         for bi in rows:
             for bj in range(_cdiv(n, TILE)):
                 units += 1
@@ -191,8 +229,8 @@ def test_oracle_pin_fails_when_a_block_mixes_shards(oracle_mod):
                 np.array_equal(scales[:1], fscale))
 
 
-def _stats(w, s=-1):
-    with wt.Plan(w, device=-1, local_shard=s) as p:
+def _stats(w, s=-1, halo=False):
+    with wt.Plan(w, device=-1, local_shard=s, halo=halo) as p:
         st = p.stats
         exp = [p.expected_count(r) for r in range(w.num_ranks)]
         lay = [p.output_layout(o, d) for o in range(len(w.outputs))
@@ -322,3 +360,148 @@ def test_two_gloo_ranks_prepare_their_own_shards(oracle_mod):
     assert sum(g["stats"]["bytes_read"] for g in gathered) == fst["bytes_read"]
     assert sum(g["stats"]["num_units"] for g in gathered) == fst["num_units"]
     assert [sum(g["expected"][r] for g in gathered) for r in range(w.num_ranks)] == fexp
+
+
+# ---- halos ------------------------------------------------------------------
+
+HALO_CASES = [(halo_mix, 4), (lambda: halo_mix(2), 2), (tiny_dense, 4), (llama_dense, 8),
+              (shard_local_mix, 4)]
+
+
+@pytest.mark.parametrize("make,shards", HALO_CASES)
+def test_halo_plans_partition_the_full_plan_and_read_only_their_halos(make, shards):
+    w = make()
+    full, full_exp, full_lay, full_pools = _stats(w)
+    tot = {k: 0 for k in ("num_units", "num_params_total", "bytes_read", "bytes_written")}
+    tot_exp = [0] * w.num_ranks
+    for s in range(shards):
+        st, exp, lay, pools = _stats(w, s, halo=True)
+        assert lay == full_lay and pools == full_pools
+        units, elems, written, per_rank = local_counts(w, s, halo=True)
+        assert (st["num_units"], st["num_params_total"], st["bytes_written"]) == (units, elems, written)
+        assert exp == per_rank
+        need = halo_rows_needed(w, s)
+        with wt.Plan(w, device=-1, local_shard=s, halo=True) as p:
+            for i, par in enumerate(w.params):
+                for k, n in enumerate(par.shard_rows):
+                    want = n if k == s else need.get((i, k), 0)
+                    assert p.shard_rows_read(i, k) == want, (par.name, k)
+                    assert want < TILE or k == s
+        for k in tot:
+            tot[k] += st[k]
+        tot_exp = [a + b for a, b in zip(tot_exp, exp)]
+    for k in tot:
+        assert tot[k] == full[k], k
+    assert tot_exp == full_exp
+
+
+def test_halo_flag_on_an_aligned_layout_equals_the_strict_plan():
+    w = kimi_k2_moe_layer(4)
+    for s in range(8):
+        assert _stats(w, s, halo=True)[:2] == _stats(w, s)[:2]
+        with wt.Plan(w, device=-1, local_shard=s, halo=True) as p:
+            assert all(p.shard_rows_read(i, k) == 0 for i in range(len(w.params))
+                       for k in range(8) if k != s)
+
+
+def test_halo_flag_alone_is_refused():
+    with pytest.raises(wt.WTError) as ei:
+        wt.Plan(halo_mix(), device=-1, flags=wt.WT_FLAG_SHARD_HALO)
+    assert ei.value.name == "WT_ERR_INVALID_ARGUMENT"
+    with wt.Plan(halo_mix(), device=-1) as p:          # a full plan reads every row
+        assert p.shard_rows_read(0, 1) == 20
+        with pytest.raises(wt.WTError):
+            p.shard_rows_read(0, 4)
+
+
+def test_halo_transfer_list():
+    w = halo_mix()
+    tr = halo_transfers(w, 4)
+    for src, dst, p, k, n in tr:
+        assert src == k != dst and 0 < n < TILE
+    for s in range(4):
+        assert {(p, k): n for src, dst, p, k, n in tr if dst == s} == halo_rows_needed(w, s)
+    assert halo_transfers(kimi_k2_moe_layer(2), 8) == []
+    with pytest.raises(ValueError):
+        halo_transfers(halo_mix(), 2)                  # shards 2 and 3 would have no rank
+
+
+def assembled_oracle_blocks(oracle_mod, w, s, rows_of):
+    """{(output, block row): (data, scale row)} of the block rows shard s
+    owns under the halo rule, computed by the oracle from the rows that
+    rows_of(param, shard, begin, end) hands out."""
+    res = {}
+    for o, out in enumerate(w.outputs):
+        m, n = w.output_shape(o)
+        own = owned_block_rows(w, o, s, halo=True)
+        if not own:
+            continue
+        pieces = []
+        for bi in own:
+            lo, hi = bi * TILE, min(m, bi * TILE + TILE)
+            for r0, cnt, p, k in all_runs(w, o):
+                a, b = max(lo, r0), min(hi, r0 + cnt)
+                if a < b:
+                    pieces.append(rows_of(p, k, a - r0, b - r0))
+        x = np.ascontiguousarray(np.concatenate(pieces, axis=0))
+        sub = Workload("local", [Param("local", x.shape[0], n, (x.shape[0],))],
+                       [Output(out.name, (0,), out.fp8, (0,))], 1, w.values)
+        data, scales = oracle_mod.Model(sub).prepare_output(0, [x])
+        esz = 1 if out.fp8 else 2
+        data = data.reshape(x.shape[0], n * esz)
+        bn = _cdiv(n, TILE)
+        for j, bi in enumerate(own):
+            h = min(TILE, m - bi * TILE)
+            srow = scales.reshape(-1, bn)[j].copy() if scales is not None else None
+            res[(o, bi)] = (data[j * TILE:j * TILE + h].copy(), srow)
+    return res
+
+
+def _halo_worker(rank, world, port, q):
+    import oracle
+    import torch
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    w = halo_mix(world)
+    full = make_shards(w)
+    own = [per[rank] for per in full]            # what this FSDP rank holds
+    del full
+    halos = exchange_halos(w, halo_transfers(w, world), rank, own)
+
+    def rows_of(p, k, a, b):
+        if k == rank:
+            t = own[p][a:b]
+        else:
+            assert b <= halos[(p, k)].shape[0], "read past the received halo"
+            t = halos[(p, k)][a:b]
+        return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+
+    local = assembled_oracle_blocks(oracle, w, rank, rows_of)
+    msg = {k: _digest(v) for k, v in local.items()}
+    gathered = [None] * world
+    dist.all_gather_object(gathered, msg)
+    if rank == 0:
+        q.put(gathered)
+    dist.barrier()
+    dist.destroy_process_group()
+
+
+def test_two_gloo_ranks_exchange_halos_and_prepare_their_blocks(oracle_mod):
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_halo_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    gathered = q.get(timeout=300)
+    for p in procs:
+        p.join(timeout=120)
+        assert p.exitcode == 0
+    w = halo_mix(2)
+    full = full_oracle_blocks(oracle_mod, w, shards_to_host_u16(make_shards(w)))
+    seen = {}
+    for g in gathered:
+        for k, h in g.items():
+            assert k not in seen
+            seen[k] = h
+    assert seen == {k: _digest(v) for k, v in full.items()}

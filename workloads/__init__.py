@@ -2,13 +2,13 @@
 their seeded source values. Shared by the tests, the benchmark and both
 sides of the parity check; holds none of the stage's arithmetic."""
 from .configs import (TILE, Output, Param, ValueRecipe, Workload, WORKLOADS, chunk_rows,
-                      edge_stress, kimi_k2_moe_layer, llama_dense, llama_dense_tp4, offload_layer,
-                      shard_local_mix, tiny_dense, tp_slices_small, tp_split)
+                      edge_stress, halo_mix, kimi_k2_moe_layer, llama_dense, llama_dense_tp4,
+                      offload_layer, shard_local_mix, tiny_dense, tp_slices_small, tp_split)
 from .values import make_shards, param_values, shards_to_host_u16, split_shards
 
 __all__ = [
     "TILE", "Output", "Param", "ValueRecipe", "Workload", "WORKLOADS", "chunk_rows",
     "edge_stress", "kimi_k2_moe_layer", "llama_dense", "llama_dense_tp4", "offload_layer",
-    "shard_local_mix", "tiny_dense", "tp_slices_small", "tp_split",
+    "halo_mix", "shard_local_mix", "tiny_dense", "tp_slices_small", "tp_split",
     "make_shards", "param_values", "shards_to_host_u16", "split_shards",
 ]

@@ -354,6 +354,31 @@ def shard_local_mix(shards: int = 4) -> Workload:
     return b.w
 
 
+def halo_mix(shards: int = 4) -> Workload:
+    """Cases for shard-local preparation with halos, where shard boundaries
+    fall off the 128-row grid: a block row spanning three shards (a 20-row
+    shard in the middle), an empty shard, a fused qkv whose parts end
+    mid-block, narrow and 16-byte rows, FP8 and BF16, dim-1 slices, a
+    replicated 1-column norm; 4 shards (2: neighbouring pairs merged),
+    3 ranks. Student-t(3) x 0.02 values, one block in eight all-zero and
+    one in eight with a +-3e4 outlier, seed 1008."""
+    splits = {"A": (100, 20, 500, 380), "q": (64, 100, 136, 0), "k": (0, 0, 72, 128),
+              "v": (50, 50, 0, 0), "emb": (175, 175, 175, 175), "norm": (75, 75, 75, 75)}
+    if shards == 2:
+        splits = {k: (v[0] + v[1], v[2] + v[3]) for k, v in splits.items()}
+    elif shards != 4:
+        raise ValueError("halo_mix has 4 or 2 shards")
+    vals = ValueRecipe("student_t3", 0.02, 1008, zero_tile_eighths=1,
+                       outlier_tile_eighths=1, outlier=3.0e4)
+    b = _Builder(f"halo_mix_s{shards}", 3, shards, vals)
+    b.output("A", [b.param("A", 1000, 2050, splits["A"])], True, (0,))
+    qkv = [b.param(n, r, 1024, splits[n]) for n, r in (("q", 300), ("k", 200), ("v", 100))]
+    b.output("qkv", qkv, True, (1, 2), slices=((1, ((0, 512),)), (1, ((512, 512),))))
+    b.output("emb", [b.param("emb", 700, 136, splits["emb"])], False, (2,))
+    b.output("norm", [b.param("norm", 300, 1, splits["norm"])], False, (0, 1))
+    return b.w
+
+
 def offload_layer(experts: int = 385, seed: int = 1005) -> Workload:
     """One layer of the streamed-offload stack: the MoE layer above plus
     attention projections q, k, v, o of 7168x7168 (q/k/v fused into qkv
@@ -374,6 +399,7 @@ WORKLOADS = {
     "llama_dense_tp4": llama_dense_tp4,
     "tp_slices_small": tp_slices_small,
     "shard_local_mix": shard_local_mix,
+    "halo_mix": halo_mix,
     "kimi_k2_moe_layer": kimi_k2_moe_layer,
     "edge_stress": edge_stress,
     "offload_layer": offload_layer,
