@@ -146,18 +146,21 @@ def max_over_ranks(world, v: float, dev) -> float:
 
 def sample_outputs(w, experts: int, target_bytes: int = 700_000_000) -> list:
     """A bounded sample of a workload's outputs: the first `experts` experts
-    of an MoE layer, else the first outputs up to about target_bytes of
-    BF16 input (at least one)."""
+    of an MoE layer, else the outputs in plan order up to about
+    target_bytes of BF16 input, skipping any single output larger than that
+    (at least one output)."""
     if w.name.startswith("kimi_k2_moe_layer"):
         return list(range(min(len(w.outputs), 2 * experts)))
     out, total = [], 0
     for o in range(len(w.outputs)):
         m, n = w.output_shape(o)
+        if 2 * m * n > target_bytes:
+            continue
         if out and total + 2 * m * n > target_bytes:
             break
         out.append(o)
         total += 2 * m * n
-    return out
+    return out or [min(range(len(w.outputs)), key=lambda o: w.output_shape(o)[0] * w.output_shape(o)[1])]
 
 
 def cpu_baseline(w_full, experts_sample: int, steps: int = 1) -> dict:
@@ -177,11 +180,27 @@ def cpu_baseline(w_full, experts_sample: int, steps: int = 1) -> dict:
         m.prepare(host, nthreads=cores)
         times.append(time.perf_counter() - t0)
     t = statistics.median(times)
+    # one thread on the first outputs of the sample (about 50 M params)
+    few, n = [], 0
+    for i, o in enumerate(outs):
+        few.append(i)
+        n += sum(sub.params[p].numel for p in sub.outputs[i].parts)
+        if n >= 50_000_000:
+            break
+    one = sub.subset(few, name=f"{sub.name}[:{len(few)}]")
+    host1 = shards_to_host_u16(make_shards(one, device="cpu"))
+    t0 = time.perf_counter()
+    oracle.Model(one).prepare(host1, nthreads=1)
+    t1 = time.perf_counter() - t0
     return {"value": round(sub.bytes_read / t / 1e9, 4), "unit": "GB/s", "cores": cores,
             "kind": "oracle", "params_per_s": round(sub.num_params_total / t, 1),
             "sample": f"{len(outs)} of {len(w_full.outputs)} outputs "
                       f"({sub.num_params_total} params, {sub.bytes_read} B BF16 in), "
-                      f"median of {steps} run(s), {t:.2f} s each"}
+                      f"median of {steps} run(s), {t:.2f} s each",
+            "single_thread": {"value": round(one.bytes_read / t1 / 1e9, 4), "unit": "GB/s", "cores": 1,
+                              "params_per_s": round(one.num_params_total / t1, 1),
+                              "sample": f"first {len(few)} outputs of that sample "
+                                        f"({one.num_params_total} params), one run, {t1:.2f} s"}}
 
 
 def run_reference(args, world, rank):

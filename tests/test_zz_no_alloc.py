@@ -87,3 +87,23 @@ def test_noalloc_rejects_schedules_beyond_its_array():
         wt.wt_prepare_noalloc(wt.PlanDesc(w), [], [0] * w.num_ranks)
     assert ei.value.name == "WT_ERR_INVALID_ARGUMENT"
     assert "at most" in str(ei.value)
+
+
+@pytest.mark.parametrize("halo", [False, True])
+def test_noalloc_runs_shard_local_plans(halo):
+    from workloads import halo_mix, shard_local_mix
+    w = halo_mix() if halo else shard_local_mix()
+    shards = make_shards(w, device="cuda:0")
+    flat = [s.data_ptr() if s.numel() else 0 for per in shards for s in per]
+    stream = torch.cuda.current_stream().cuda_stream
+    for s in range(4):
+        plan = wt.Plan(w, device=0, local_shard=s, halo=halo)
+        want = _pools(plan, w.num_ranks, CANARY)
+        plan.prepare(flat, [p.data_ptr() for p in want], stream)
+        got = _pools(plan, w.num_ranks, CANARY)
+        wt.wt_prepare_noalloc(wt.PlanDesc(w, local_shard=s, halo=halo), flat,
+                              [p.data_ptr() for p in got], stream)
+        torch.cuda.synchronize()
+        for r in range(w.num_ranks):
+            assert torch.equal(got[r], want[r]), (s, r)
+        plan.close()
