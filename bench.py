@@ -47,8 +47,8 @@ L2_BYTES = 126 * 10**6
 # from the ncu capture summarised in profiles/ (16 experts, scaled by the
 # blocks processed to the 385-expert layer); valid only for the kernel
 # source it was taken on.
-TRAFFIC = {"kernel_sha256": "1107121017daa12244f3b3923b714ae5e8d622e6d4e53d26df6f54e23e3cb7d8",
-           "bytes_per_launch": 49560372400, "experts": 385}
+TRAFFIC = {"kernel_sha256": "e5c00528b381e0e7881a4e0681193e0787170841f70486aaaac395c562f1082e",
+           "bytes_per_launch": 50018374560, "experts": 385}
 
 
 def kernel_sha() -> str:
