@@ -358,35 +358,93 @@ __device__ void gather_stage(const PrepArgs& a, const DevUnit& m, uint8_t* sp, i
                 (int64_t)m.bj * kTile;
   }
   for (int rb = wg; rb < kTile; rb += kGroupWarps * kRowsAtOnce) {
-    uint16_t e[kRowsAtOnce][kTile / 32];
+    // lane l takes the element pairs l and l + 32 of each row: one 4-byte
+    // load where the row start is 4-byte aligned (an even row length in a
+    // 4-byte aligned shard), else two 2-byte loads; nothing past column
+    // ncols - 1 is read
+    uint32_t e[kRowsAtOnce][kTile / 64];
 #pragma unroll
     for (int i = 0; i < kRowsAtOnce; ++i) {
       const int r = rb + i * kGroupWarps;
       const uint16_t* row = r < nrows ? gather_row(a, m, run, one_shard, r) : nullptr;
+      const bool w4 = row && (reinterpret_cast<uintptr_t>(row) & 3u) == 0;
 #pragma unroll
-      for (int c4 = 0; c4 < kTile / 32; ++c4) {
-        const int c = lane + 32 * c4;
-        e[i][c4] = (row && c < ncols) ? ld_nc_u16(row + c) : (uint16_t)0;
+      for (int c2 = 0; c2 < kTile / 64; ++c2) {
+        const int c = 2 * (lane + 32 * c2);
+        if (w4 && c + 1 < ncols) {
+          e[i][c2] = ld_nc_u32(row + c);
+        } else {
+          const uint32_t lo = (row && c < ncols) ? ld_nc_u16(row + c) : 0u;
+          const uint32_t hi = (row && c + 1 < ncols) ? ld_nc_u16(row + c + 1) : 0u;
+          e[i][c2] = lo | (hi << 16);
+        }
       }
     }
 #pragma unroll
     for (int i = 0; i < kRowsAtOnce; ++i) {
-      uint16_t* out = reinterpret_cast<uint16_t*>(sp + (rb + i * kGroupWarps) * kRowBytes);
+      uint32_t* out = reinterpret_cast<uint32_t*>(sp + (rb + i * kGroupWarps) * kRowBytes);
 #pragma unroll
-      for (int c4 = 0; c4 < kTile / 32; ++c4) out[lane + 32 * c4] = e[i][c4];
+      for (int c2 = 0; c2 < kTile / 64; ++c2) out[lane + 32 * c2] = e[i][c2];
     }
   }
 }
 
-// Codes of one row chunk, byte by byte (outputs whose rows are not 8-byte
-// aligned); `valid` bytes of the 8 are inside the block.
+// Codes of one row chunk where rows are not 8-byte aligned; `valid` bytes
+// of the 8 are inside the block. A whole chunk goes out in the widest
+// stores its address allows (rows of an even length are 2-byte aligned,
+// every fourth one 8-byte aligned), a partial one byte by byte.
 template <bool kDebug>
 __device__ __forceinline__ void store_codes_bytes(const PrepArgs& a, const DevDstPtr& dp, uint8_t* p, uint2 q,
                                                   bool row_ok, int valid) {
+  if (!row_ok) return;
   const uint32_t wds[2] = {q.x, q.y};
+  const uintptr_t al = reinterpret_cast<uintptr_t>(p);
+  if (valid >= 8 && (al & 1u) == 0) {
+    if (!store_ok<kDebug>(a, dp, p, 8)) return;
+    if ((al & 7u) == 0) {
+      *reinterpret_cast<uint2*>(p) = q;
+    } else if ((al & 3u) == 0) {
+      reinterpret_cast<uint32_t*>(p)[0] = q.x;
+      reinterpret_cast<uint32_t*>(p)[1] = q.y;
+    } else {
+#pragma unroll
+      for (int h = 0; h < 4; ++h) reinterpret_cast<uint16_t*>(p)[h] = (uint16_t)(wds[h >> 1] >> (16 * (h & 1)));
+    }
+    return;
+  }
 #pragma unroll
   for (int e = 0; e < 8; ++e)
-    if (row_ok && e < valid && store_ok<kDebug>(a, dp, p + e, 1)) p[e] = (uint8_t)(wds[e >> 2] >> (8 * (e & 3)));
+    if (e < valid && store_ok<kDebug>(a, dp, p + e, 1)) p[e] = (uint8_t)(wds[e >> 2] >> (8 * (e & 3)));
+}
+
+// Eight BF16 values of one row chunk where rows are not 16-byte aligned
+// (always 2-byte aligned): the widest stores the address allows for a
+// whole chunk, element by element for a partial one.
+template <bool kDebug>
+__device__ __forceinline__ void store_bf16_chunk(const PrepArgs& a, const DevDstPtr& dp, uint8_t* p, uint4 v,
+                                                 int valid) {
+  const uint32_t wds[4] = {v.x, v.y, v.z, v.w};
+  const uintptr_t al = reinterpret_cast<uintptr_t>(p);
+  if (valid >= 8) {
+    if (!store_ok<kDebug>(a, dp, p, 16)) return;
+    if ((al & 15u) == 0) {
+      *reinterpret_cast<uint4*>(p) = v;
+    } else if ((al & 7u) == 0) {
+      reinterpret_cast<uint2*>(p)[0] = make_uint2(v.x, v.y);
+      reinterpret_cast<uint2*>(p)[1] = make_uint2(v.z, v.w);
+    } else if ((al & 3u) == 0) {
+#pragma unroll
+      for (int k = 0; k < 4; ++k) reinterpret_cast<uint32_t*>(p)[k] = wds[k];
+    } else {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) reinterpret_cast<uint16_t*>(p)[e] = (uint16_t)(wds[e >> 1] >> (16 * (e & 1)));
+    }
+    return;
+  }
+#pragma unroll
+  for (int e = 0; e < 8; ++e)
+    if (e < valid && store_ok<kDebug>(a, dp, p + 2 * e, 2))
+      *reinterpret_cast<uint16_t*>(p + 2 * e) = (uint16_t)(wds[e >> 1] >> (16 * (e & 1)));
 }
 
 // The general FP8 path (partial blocks, rows that are not 16-byte aligned,
@@ -446,11 +504,7 @@ __device__ __noinline__ void store_bf16_general(const PrepArgs& a, const DevUnit
       if (vec) {
         if (store_ok<kDebug>(a, dp, p, 16)) *reinterpret_cast<uint4*>(p) = v;
       } else {
-        const uint32_t wds[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int e = 0; e < 8; ++e)
-          if (cc * 8 + e < ncols && store_ok<kDebug>(a, dp, p + 2 * e, 2))
-            *reinterpret_cast<uint16_t*>(p + 2 * e) = (uint16_t)(wds[e >> 1] >> (16 * (e & 1)));
+        store_bf16_chunk<kDebug>(a, dp, p, v, ncols - cc * 8);
       }
     }
   }
