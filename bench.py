@@ -144,6 +144,16 @@ def max_over_ranks(world, v: float, dev) -> float:
     return float(t.item())
 
 
+def sum_over_ranks(world, v: float, dev) -> float:
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
 def sample_outputs(w, experts: int, target_bytes: int = 700_000_000) -> list:
     """A bounded sample of a workload's outputs: the first `experts` experts
     of an MoE layer, else the outputs in plan order up to about
@@ -357,8 +367,12 @@ def main():
     total_ms = starts[0].elapsed_time(ends[-1])
     total_ms = max_over_ranks(world, total_ms, dev)
     ms_per_step = total_ms / args.steps
-    value = world * st["bytes_read"] / (ms_per_step * 1e-3) / 1e9
-    params_per_s = world * st["num_params_total"] / (ms_per_step * 1e-3)
+    # the units every rank processed (replicas: each a whole layer; shard-local:
+    # each its own share of one layer)
+    job_bytes = sum_over_ranks(world, st["bytes_read"], dev)
+    job_params = sum_over_ranks(world, st["num_params_total"], dev)
+    value = job_bytes / (ms_per_step * 1e-3) / 1e9
+    params_per_s = job_params / (ms_per_step * 1e-3)
     avg_launch_s = statistics.mean(per_launch_ms) * 1e-3
     alg_bytes = st["bytes_read"] + st["bytes_written"]
     peaks = measured_peaks()
