@@ -47,8 +47,8 @@ L2_BYTES = 126 * 10**6
 # from the ncu capture summarised in profiles/ (16 experts, scaled by the
 # blocks processed to the 385-expert layer); valid only for the kernel
 # source it was taken on.
-TRAFFIC = {"kernel_sha256": "e5c00528b381e0e7881a4e0681193e0787170841f70486aaaac395c562f1082e",
-           "bytes_per_launch": 50018374560, "experts": 385}
+TRAFFIC = {"kernel_sha256": "756562425cc6dcdd71b41e3b65a5be7d02a3faa9006dedfc035c6640282e4ed7",
+           "bytes_per_launch": 50000621440, "experts": 385}
 
 
 def kernel_sha() -> str:
