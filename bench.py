@@ -68,6 +68,16 @@ def measured_peaks() -> dict:
         return {}
 
 
+def gpu_bus_id(dev) -> str | None:
+    """PCI bus id of the device, as nvidia-smi --id takes it."""
+    import torch
+    props = torch.cuda.get_device_properties(dev)
+    try:
+        return f"{props.pci_domain_id:08X}:{props.pci_bus_id:02X}:{props.pci_device_id:02X}.0"
+    except AttributeError:
+        return None
+
+
 class ClockSampler:
     """nvidia-smi samples of SM clock and throttle reasons while running."""
 
@@ -342,12 +352,7 @@ def main():
             plan.prepare(shard_ptrs, pool_ptrs, sp)
     stream.synchronize()
 
-    props = torch.cuda.get_device_properties(dev)
-    bus = None
-    try:
-        bus = f"{props.pci_domain_id:08X}:{props.pci_bus_id:02X}:{props.pci_device_id:02X}.0"
-    except AttributeError:
-        pass
+    bus = gpu_bus_id(dev)
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     barrier(world)
@@ -440,7 +445,9 @@ def main():
         "first_step_host_ms": round(first_step_host_ms, 2), "shards": st["num_slots"],
         "completion_counters": args.counters,
         "e2e": e2e, "cpu_baseline": cpu, "clocks": clk,
-        "gpu_launches": args.steps, "wall_s_timed": round(t_wall, 4),
+        # the preparation kernel, plus the count kernel when counting per launch
+        "gpu_launches": args.steps * (2 if args.counters == "launch" else 1),
+        "wall_s_timed": round(t_wall, 4),
     }
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -484,7 +491,7 @@ def run_tokens(args, world, rank, local):
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     barrier(world)
     torch.cuda.synchronize(dev)
-    clocks = ClockSampler(None)
+    clocks = ClockSampler(gpu_bus_id(dev))
     time.sleep(0.3)
     for i in range(args.steps):
         starts[i].record(stream)
@@ -642,10 +649,13 @@ def run_offload_stack(args, world, rank, local):
     for _ in range(args.stack_warmup):
         step()
     barrier(world)
+    clocks = ClockSampler(gpu_bus_id(dev))
+    time.sleep(0.3)
     t0 = time.perf_counter()
     for _ in range(args.stack_steps):
         step()
     dt = (time.perf_counter() - t0) / args.stack_steps
+    clk = clocks.stop()
     dt = max_over_ranks(world, dt, dev)
     peak = h2d_peak(images[0], dev, copy_s)
     plan.close()
@@ -665,6 +675,9 @@ def run_offload_stack(args, world, rank, local):
                 "d2h_bytes_per_step": 4},
         "h2d_peak_gbs": round(peak, 2),
         "overlap_efficiency": round(host_bytes / (peak * 1e9) / dt, 4),
+        "clocks": clk,
+        # one preparation launch per chunk of every layer
+        "gpu_launches": args.stack_steps * layers * st["num_chunks"],
     }
     if rank == 0:
         print(json.dumps(line), flush=True)
