@@ -280,6 +280,8 @@ def main():
     ap.add_argument("--shard-local", action="store_true",
                     help="FSDP group of --fsdp ranks sharing one layer; each prepares its own shard")
     ap.add_argument("--fsdp", type=int, default=0, help="FSDP degree for --shard-local (0: world)")
+    ap.add_argument("--halo", action="store_true",
+                    help="with --shard-local: shard boundaries off the 128-row grid, halo rows exchanged")
     ap.add_argument("--counters", choices=["launch", "block"], default=None,
                     help="time the step with per-rank completion counters")
     ap.add_argument("--tokens", type=int, default=131072)
@@ -312,23 +314,47 @@ def main():
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     fsdp = (args.fsdp or world) if args.shard_local else 0
+    if args.halo and not args.shard_local:
+        ap.error("--halo needs --shard-local")
     if args.shard_local:
-        if args.workload != "kimi_k2_moe_layer" or rank >= fsdp:
-            ap.error("--shard-local runs the Kimi-K2 layer with --fsdp >= the world size")
-        # one layer shared by the group: every rank draws the same values
-        w = kimi_k2_moe_layer(args.experts, shards=fsdp)
+        # one model shared by the group: every rank draws the same values
+        if args.workload == "kimi_k2_moe_layer":
+            w = kimi_k2_moe_layer(args.experts, shards=fsdp)
+        elif args.workload in ("offload_8layer", "tokens"):
+            ap.error("--shard-local prepares a plan workload")
+        else:
+            w = WORKLOADS[args.workload]()
+            if any(len(p.shard_rows) != fsdp for p in w.params):
+                ap.error(f"{w.name} has {len(w.params[0].shard_rows)} shards per weight: use that --fsdp")
+        if rank >= fsdp:
+            ap.error("--fsdp must be at least the world size")
     elif args.workload == "kimi_k2_moe_layer":
         w = kimi_k2_moe_layer(args.experts, seed=1003 + rank)
     else:
         w = WORKLOADS[args.workload]()
+    plan = wt.Plan(w, device=local, local_shard=rank if args.shard_local else -1, halo=args.halo)
     shards = make_shards(w, device=dev)
+    halo_bytes = 0
     if args.shard_local:
-        # this rank keeps its own shard of every weight and nothing else
-        shards = [[s if k == rank else s.new_empty(0) for k, s in enumerate(per)] for per in shards]
+        # this rank keeps its own shard of every weight, plus the halo rows
+        # its plan reads from other shards: received from their ranks under
+        # torchrun, cut from the locally drawn copy at one GPU
+        need = {(i, k): plan.shard_rows_read(i, k) for i, per in enumerate(shards)
+                for k in range(len(per)) if k != rank}
+        if world > 1 and args.halo:
+            if fsdp != world:
+                ap.error("exchanging halos needs --fsdp equal to the world size")
+            from bf16_fp8_parameter_wt_b300.schedule import exchange_halos, halo_transfers
+            barrier(world)                     # a collective before the first point-to-point batch
+            got = exchange_halos(w, halo_transfers(w, fsdp), rank, [per[rank] for per in shards])
+        else:
+            got = {key: shards[key[0]][key[1]][:n].clone() for key, n in need.items() if n}
+        shards = [[s if k == rank else got.get((i, k), s.new_empty(0)) for k, s in enumerate(per)]
+                  for i, per in enumerate(shards)]
+        halo_bytes = sum(t.numel() * 2 for t in got.values())
         torch.cuda.empty_cache()
     flat = [s for per in shards for s in per]
     shard_ptrs = [s.data_ptr() if s.numel() else 0 for s in flat]
-    plan = wt.Plan(w, device=local, local_shard=rank if args.shard_local else -1)
     st = plan.stats
     pools = [torch.empty(max(1, plan.pool_bytes(r)), dtype=torch.uint8, device=dev)
              for r in range(w.num_ranks)]
@@ -439,6 +465,7 @@ def main():
                    "l2": (f"inputs ({st['bytes_read'] / 1e9:.1f} GB) larger than the 126 MB L2, no flush"
                           if st["bytes_read"] > L2_BYTES else
                           "inputs smaller than L2: L2-resident, a latency figure"),
+                   "halo_bytes_per_rank": halo_bytes if args.shard_local else None,
                    "parallelism": (f"shard-local rank {rank} of an FSDP group of {fsdp}" if args.shard_local
                                    else f"replicas x{world}" if world > 1 else "single")},
         "roofline": roofline, "graph_replay_us": graph_us,

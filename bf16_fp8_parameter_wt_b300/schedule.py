@@ -84,19 +84,23 @@ def exchange_halos(w, transfers, rank: int, own_shards, group=None) -> dict:
     {(param, shard): [rows, cols] tensor} of the received halo rows."""
     import torch
     import torch.distributed as dist
-    reqs, keep, got = [], [], {}
+    ops, got = [], {}
     dev = next((t.device for t in own_shards if t is not None), torch.device("cpu"))
     # raw 16-bit payloads (no reduction happens, so the dtype is only a
-    # size); one tag per transfer so that messages pair up unambiguously
+    # size); every rank walks the same list in the same order, so sends
+    # and receives pair up, and one tag per transfer where the backend
+    # uses tags; posted as one batch (a group of point-to-point calls for
+    # NCCL, where separately posted sends and receives can wait on each
+    # other)
     for tag, (src, dst, p, k, n) in enumerate(transfers):
         if src == rank and dst != rank:
             t = own_shards[p][:n].contiguous().view(torch.int16)
-            keep.append(t)
-            reqs.append(dist.isend(t, dst, group=group, tag=tag))
+            ops.append(dist.P2POp(dist.isend, t, dst, group=group, tag=tag))
         elif dst == rank and src != rank:
             buf = torch.empty((n, w.params[p].cols), dtype=torch.int16, device=dev)
             got[(p, k)] = buf.view(torch.bfloat16)
-            reqs.append(dist.irecv(buf, src, group=group, tag=tag))
-    for q in reqs:
-        q.wait()
+            ops.append(dist.P2POp(dist.irecv, buf, src, group=group, tag=tag))
+    if ops:
+        for q in dist.batch_isend_irecv(ops):
+            q.wait()
     return got
