@@ -8,6 +8,8 @@
 #include <new>
 #include <string>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "plan.h"
 
 namespace wt {
@@ -26,6 +28,14 @@ struct DeviceGuard {
     int cur = -1;
     if (prev >= 0 && cudaGetDevice(&cur) == cudaSuccess && cur != prev) cudaSetDevice(prev);
   }
+};
+
+// An NVTX range over one host-side entry point (plan compilation, the
+// queueing of a step), for timelines taken with a profiler; without one
+// attached the calls do nothing.
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
 };
 
 wt_status fail(wt_status s, const std::string& msg) {
@@ -70,6 +80,14 @@ DynLayout dyn_layout(const Plan& p) {
   return d;
 }
 
+// A failed allocation leaves its (non-sticky) error as the runtime's last
+// error; take it back so that a later call's launch check does not report
+// it as its own failure.
+wt_status alloc_fail(const char* what) {
+  (void)cudaGetLastError();
+  return fail(WT_ERR_OUT_OF_MEMORY, what);
+}
+
 // Upload the static tables and allocate what the per-step calls need, so
 // that wt_prepare and wt_prepare_offload never allocate.
 wt_status upload(Plan& p, int device) {
@@ -108,7 +126,7 @@ wt_status upload(Plan& p, int device) {
   const size_t o_offl_s = take(offload ? n_slots * sizeof(void*) : 0);
   const size_t o_offl_t = take(offload ? n_slots * kTmapBytes : 0);
   e = cudaMalloc(&p.d_tables, std::max<size_t>(off, 256));
-  if (e != cudaSuccess) return fail(WT_ERR_OUT_OF_MEMORY, "cudaMalloc of plan tables failed");
+  if (e != cudaSuccess) return alloc_fail("cudaMalloc of plan tables failed");
   char* base = static_cast<char*>(p.d_tables);
   auto put = [&](size_t o, const void* src, size_t bytes) {
     return bytes ? cudaMemcpy(base + o, src, bytes, cudaMemcpyHostToDevice) : cudaSuccess;
@@ -138,7 +156,7 @@ wt_status upload(Plan& p, int device) {
   p.args.timeout_ns = kDefaultTimeoutNs;
 
   e = cudaHostAlloc(&p.h_pinned, std::max<size_t>(dl.bytes, 256), cudaHostAllocDefault);
-  if (e != cudaSuccess) return fail(WT_ERR_OUT_OF_MEMORY, "pinned pointer staging allocation failed");
+  if (e != cudaSuccess) return alloc_fail("pinned pointer staging allocation failed");
   std::memset(p.h_pinned, 0, std::max<size_t>(dl.bytes, 256));
   if ((e = cudaEventCreateWithFlags(&p.ptr_upload_done, cudaEventDisableTiming)) != cudaSuccess ||
       (e = cudaEventCreateWithFlags(&p.last_done, cudaEventDisableTiming)) != cudaSuccess)
@@ -151,7 +169,7 @@ wt_status upload(Plan& p, int device) {
     // the watermark: two staging buffers of the largest chunk
     for (int b = 0; b < 2; ++b) {
       if (p.staging_bytes && cudaMalloc(&p.staging[b], p.staging_bytes) != cudaSuccess)
-        return fail(WT_ERR_OUT_OF_MEMORY, "offload staging allocation failed");
+        return alloc_fail("offload staging allocation failed");
       if ((e = cudaEventCreateWithFlags(&p.h2d_done[b], cudaEventDisableTiming)) != cudaSuccess ||
           (e = cudaEventCreateWithFlags(&p.prep_done[b], cudaEventDisableTiming)) != cudaSuccess)
         return cuda_fail(e, "cudaEventCreate");
@@ -274,6 +292,7 @@ using namespace wt;
 extern "C" {
 
 wt_status wt_plan_create(const wt_plan_desc* desc, int device, wt_plan** out) {
+  NvtxRange range("wt_plan_create");
   if (!out) return fail(WT_ERR_INVALID_ARGUMENT, "out is NULL");
   if (device < -1) return fail(WT_ERR_INVALID_ARGUMENT, "device must be >= -1");
   wt_plan* h = new (std::nothrow) wt_plan;
@@ -346,6 +365,7 @@ wt_status wt_plan_get_stats(const wt_plan* h, wt_plan_stats* st) {
 }
 
 wt_status wt_prepare(wt_plan* h, const void* const* shard_ptrs, void* const* pools, void* stream) {
+  NvtxRange range("wt_prepare");
   if (!h) return fail(WT_ERR_INVALID_ARGUMENT, "plan is NULL");
   Plan& p = h->p;
   if (p.device < 0) return fail(WT_ERR_INVALID_ARGUMENT, "host-only plan cannot run");
@@ -383,6 +403,7 @@ wt_status wt_prepare(wt_plan* h, const void* const* shard_ptrs, void* const* poo
 
 wt_status wt_prepare_offload(wt_plan* h, const void* host_image, void* const* pools,
                              void* copy_stream, void* compute_stream) {
+  NvtxRange range("wt_prepare_offload");
   if (!h) return fail(WT_ERR_INVALID_ARGUMENT, "plan is NULL");
   Plan& p = h->p;
   if (p.device < 0) return fail(WT_ERR_INVALID_ARGUMENT, "host-only plan cannot run");

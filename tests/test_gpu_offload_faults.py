@@ -111,3 +111,21 @@ def test_stalled_wait_reports_timeout_then_recovers(oracle_mod, make, unit):
     plan.check()
     assert_pools_equal(pools, want)
     plan.close()
+
+
+def test_allocation_failure_is_reported_and_leaves_no_stale_error(oracle_mod):
+    """Offload staging larger than the GPU (two buffers of a 300 GB chunk):
+    the plan is refused with WT_ERR_OUT_OF_MEMORY, its tables are freed, and
+    the failed cudaMalloc does not surface as an error of the next plan's
+    step."""
+    from gpu_helpers import full_check
+    from workloads import Output, Param, Workload
+    huge = Workload("huge", [Param("x", 150_000, 1_000_000, (150_000,))],
+                    [Output("x", (0,), True, (0,))], 1)
+    free0 = torch.cuda.mem_get_info(0)[0]
+    with pytest.raises(wt.WTError) as ei:
+        wt.Plan(huge, device=0, offload_chunk_bytes=1 << 40)
+    assert ei.value.name == "WT_ERR_OUT_OF_MEMORY"
+    assert "offload staging" in str(ei.value)
+    assert torch.cuda.mem_get_info(0)[0] >= free0 - (64 << 20)     # nothing left behind
+    full_check(oracle_mod, tiny_dense())
