@@ -14,13 +14,13 @@ full_tensor() gather is what the shortcut avoids).
   bytes, element counts and per-rank expected blocks add up to the full
   plan's, the layout is the full plan's, and the counts match an
   ownership count made here from the workload.
-- Two gloo ranks each compile their own local plan and run the oracle on
+- Two or four gloo ranks each compile their own local plan and run the oracle on
   their own shards only; rank 0 checks the union against the full oracle.
 - Misaligned shards, offload and bad arguments are refused.
 - With halos (WT_FLAG_SHARD_HALO) boundaries may be off the grid: a block
   row belongs to the shard holding its first row, and the plan reports,
   per shard, the leading rows it reads; those match a count made here,
-  the local plans still partition the full plan, and two gloo ranks that
+  the local plans still partition the full plan, and two or four gloo ranks that
   exchange exactly those rows (schedule.exchange_halos) and run the
   oracle on what they hold reproduce the full oracle output.
 """
@@ -186,7 +186,7 @@ def test_bad_shard_local_arguments():
     wt.wt_plan_destroy(h.value)
 
 
-# ---- two gloo ranks, each with its own shard ------------------------------
+# ---- gloo ranks, each with its own shard -----------------------------------
 
 def _free_port():
     sk = socket.socket()
@@ -228,18 +228,19 @@ def _worker(rank, world, port, q):
     dist.destroy_process_group()
 
 
-def test_two_gloo_ranks_prepare_their_own_shards(oracle_mod):
+@pytest.mark.parametrize("world", [2, 4])
+def test_gloo_ranks_prepare_their_own_shards(oracle_mod, world):
     ctx = mp.get_context("spawn")
     q = ctx.Queue()
     port = _free_port()
-    procs = [ctx.Process(target=_worker, args=(r, 2, port, q)) for r in range(2)]
+    procs = [ctx.Process(target=_worker, args=(r, world, port, q)) for r in range(world)]
     for p in procs:
         p.start()
     gathered = q.get(timeout=300)
     for p in procs:
         p.join(timeout=120)
         assert p.exitcode == 0
-    w = shard_local_mix(2)
+    w = shard_local_mix(world)
     full = full_oracle_blocks(oracle_mod, w, shards_to_host_u16(make_shards(w)))
     seen = {}
     for g in gathered:
@@ -346,18 +347,21 @@ def _halo_worker(rank, world, port, q):
     dist.destroy_process_group()
 
 
-def test_two_gloo_ranks_exchange_halos_and_prepare_their_blocks(oracle_mod):
+@pytest.mark.parametrize("world", [2, 4])
+def test_gloo_ranks_exchange_halos_and_prepare_their_blocks(oracle_mod, world):
+    # world 4: block row 0 of A starts in shard 0 and runs through the
+    # 20-row shard 1 into shard 2, so rank 0 receives from two ranks
     ctx = mp.get_context("spawn")
     q = ctx.Queue()
     port = _free_port()
-    procs = [ctx.Process(target=_halo_worker, args=(r, 2, port, q)) for r in range(2)]
+    procs = [ctx.Process(target=_halo_worker, args=(r, world, port, q)) for r in range(world)]
     for p in procs:
         p.start()
     gathered = q.get(timeout=300)
     for p in procs:
         p.join(timeout=120)
         assert p.exitcode == 0
-    w = halo_mix(2)
+    w = halo_mix(world)
     full = full_oracle_blocks(oracle_mod, w, shards_to_host_u16(make_shards(w)))
     seen = {}
     for g in gathered:
