@@ -1,0 +1,29 @@
+"""Host-side pieces of bench.py (no GPU): the bounded CPU-oracle sample, the
+CPU-baseline record and the single-rank reductions."""
+import bench
+from workloads import edge_stress, kimi_k2_moe_layer, llama_dense, tiny_dense
+
+
+def test_sample_outputs_are_bounded_and_representative():
+    k = kimi_k2_moe_layer()
+    assert bench.sample_outputs(k, 8) == list(range(16))           # the first 8 experts
+    for w in (llama_dense(), edge_stress(), tiny_dense()):
+        outs = bench.sample_outputs(w, 8)
+        assert outs and len(set(outs)) == len(outs)
+        total = sum(2 * w.output_shape(o)[0] * w.output_shape(o)[1] for o in outs)
+        assert total <= 700_000_000
+    # the dense stack's sample is its layers, not its 1 GB embedding alone
+    l = llama_dense()
+    assert [l.outputs[o].name for o in bench.sample_outputs(l, 8)][:2] == ["l0.qkv", "l0.o"]
+
+
+def test_cpu_baseline_record(oracle_mod):
+    rec = bench.cpu_baseline(tiny_dense(), 8)
+    assert rec["kind"] == "oracle" and rec["unit"] == "GB/s" and rec["value"] > 0
+    assert rec["cores"] >= 1 and rec["single_thread"]["cores"] == 1
+    assert "15 of 15 outputs" in rec["sample"]
+
+
+def test_single_rank_reductions_are_identities():
+    assert bench.max_over_ranks(1, 3.5, None) == 3.5
+    assert bench.sum_over_ranks(1, 7.0, None) == 7.0
