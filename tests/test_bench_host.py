@@ -27,3 +27,18 @@ def test_cpu_baseline_record(oracle_mod):
 def test_single_rank_reductions_are_identities():
     assert bench.max_over_ranks(1, 3.5, None) == 3.5
     assert bench.sum_over_ranks(1, 7.0, None) == 7.0
+
+
+def test_end_to_end_leg_fits_the_pinned_budget():
+    import bf16_fp8_parameter_wt_b300 as wt
+    w = kimi_k2_moe_layer()
+    shards = [[None] * len(p.shard_rows) for p in w.params]
+    with wt.Plan(w, device=-1, offload_chunk_bytes=2 << 30) as p:
+        full = p.stats["host_bytes"]
+    assert bench.e2e_subset(w, shards, full, full)[2] is None          # fits: the whole layer
+    sub, sh, note = bench.e2e_subset(w, shards, full, full / 8)
+    assert note and len(sh) == len(sub.params) and sub.params == w.params[:len(sh)]
+    with wt.Plan(sub, device=-1, offload_chunk_bytes=2 << 30) as p:
+        assert p.stats["host_bytes"] <= full / 8
+    assert len(sub.outputs) == 2 * (385 // 8)
+    assert bench.e2e_subset(llama_dense(), [], 10 ** 12, 1.0)[2] is None   # only the MoE layer is cut
