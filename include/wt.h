@@ -163,7 +163,10 @@ typedef struct {
    * of the next shards; excludes offload_chunk_bytes. Layout, pool sizes and
    * host offsets are those of the full plan; stats, expected counts and
    * the units run are the local ones; shard pointers of other indices may
-   * be NULL (see wt_plan_shard_rows_read). */
+   * be NULL (see wt_plan_shard_rows_read). WT_ERR_INVALID_ARGUMENT for a
+   * negative local_shard, for offload_chunk_bytes > 0, or for
+   * WT_FLAG_SHARD_HALO without WT_FLAG_SHARD_LOCAL; a local_shard past a
+   * parameter's last shard simply selects none of its rows. */
   int32_t local_shard;
 } wt_plan_desc;
 
