@@ -8,7 +8,7 @@ from .wt import (EXPORTS, LIB_PATH, WT_COUNT_PER_BLOCK, WT_COUNT_PER_LAUNCH, WT_
                  wt_last_error, wt_plan_check, wt_plan_create, wt_plan_destroy,
                  wt_plan_expected_count, wt_plan_get_stats, wt_plan_output_layout,
                  wt_plan_pool_bytes, wt_plan_set_counters, wt_plan_shard_host_offset, wt_plan_shard_rows_read, wt_prepare,
-                 wt_prepare_noalloc, wt_prepare_offload, wt_quantize_tokens, wt_status_string,
+                 wt_debug_noalloc_stall_unit, wt_noalloc_check, wt_prepare_noalloc, wt_prepare_offload, wt_quantize_tokens, wt_status_string,
                  wt_wait_counters)
 
 __all__ = [
@@ -17,7 +17,7 @@ __all__ = [
     "WT_OUT_BF16", "WT_OUT_FP8_E4M3_B128", "Plan", "PlanDesc", "WTError", "lib",
     "wt_debug_fail_offload_chunk", "wt_debug_stall_unit", "wt_last_error", "wt_plan_check", "wt_plan_create",
     "wt_plan_destroy", "wt_plan_get_stats", "wt_plan_output_layout", "wt_plan_pool_bytes",
-    "wt_plan_shard_host_offset", "wt_plan_shard_rows_read", "wt_prepare", "wt_plan_expected_count", "wt_plan_set_counters", "wt_prepare_noalloc",
+    "wt_plan_shard_host_offset", "wt_plan_shard_rows_read", "wt_prepare", "wt_plan_expected_count", "wt_plan_set_counters", "wt_prepare_noalloc", "wt_noalloc_check", "wt_debug_noalloc_stall_unit",
     "wt_prepare_offload", "wt_quantize_tokens", "wt_wait_counters",
     "wt_status_string",
 ]

@@ -30,7 +30,7 @@ WT_FLAG_SHARD_HALO = 0x8
 EXPORTS = ["wt_plan_create", "wt_plan_pool_bytes", "wt_plan_output_layout",
            "wt_plan_shard_host_offset", "wt_plan_shard_rows_read", "wt_plan_get_stats", "wt_prepare", "wt_prepare_offload",
            "wt_plan_check", "wt_debug_fail_offload_chunk", "wt_debug_stall_unit", "wt_plan_destroy",
-           "wt_prepare_noalloc", "wt_quantize_tokens", "wt_plan_set_counters",
+           "wt_prepare_noalloc", "wt_noalloc_check", "wt_debug_noalloc_stall_unit", "wt_quantize_tokens", "wt_plan_set_counters",
            "wt_plan_expected_count", "wt_wait_counters",
            "wt_status_string", "wt_last_error"]
 
@@ -96,6 +96,8 @@ def lib() -> C.CDLL:
         L.wt_prepare.argtypes = [P, P, P, P]
         L.wt_prepare_offload.argtypes = [P, P, P, P, P]
         L.wt_prepare_noalloc.argtypes = [C.POINTER(wt_plan_desc), P, P, P]
+        L.wt_noalloc_check.argtypes = [P]
+        L.wt_debug_noalloc_stall_unit.argtypes = [C.c_int64, C.c_uint64]
         L.wt_plan_check.argtypes = [P, P]
         L.wt_debug_fail_offload_chunk.argtypes = [P, C.c_int32]
         L.wt_debug_stall_unit.argtypes = [P, C.c_int64, C.c_uint64]
@@ -246,6 +248,16 @@ def wt_prepare_noalloc(desc: "PlanDesc", shard_ptrs: Sequence[int], pools: Seque
     scratch array. Calls overlapping on the GPU share that array and race."""
     _check(lib().wt_prepare_noalloc(C.byref(desc.c), _ptr_array(shard_ptrs), _ptr_array(pools),
                                     stream or None))
+
+
+def wt_noalloc_check(stream: int = 0) -> None:
+    """Synchronise `stream` and report (then clear) a wait that gave up in an
+    earlier wt_prepare_noalloc kernel on the current device."""
+    _check(lib().wt_noalloc_check(stream or None))
+
+
+def wt_debug_noalloc_stall_unit(unit: int, wait_limit_ns: int = 0) -> None:
+    _check(lib().wt_debug_noalloc_stall_unit(unit, wait_limit_ns))
 
 
 def wt_plan_check(plan: int, stream: int = 0) -> None:

@@ -194,10 +194,20 @@ typedef struct {
  * WT_ERR_OUT_OF_MEMORY, WT_ERR_CUDA. */
 wt_status wt_plan_create(const wt_plan_desc* desc, int device, wt_plan** out);
 
-/* Bytes the pool of `rank` must hold (0 for a rank with no destination). */
+/* Bytes the pool of `rank` must hold (0 for a rank with no destination).
+ * The pool is the destination memory region of "Weight transfer for RL
+ * post-training in under 2 seconds", section "RDMA WRITE: one-sided
+ * transfers" (the inference side registers it once; every write lands at
+ * an offset in it). Errors: WT_ERR_INVALID_ARGUMENT (NULL plan or out
+ * pointer, rank out of range). */
 wt_status wt_plan_pool_bytes(const wt_plan* p, int32_t rank, uint64_t* bytes);
 
-/* Resolved destination `dst` of output `out`. */
+/* Resolved destination `dst` of output `out`: the rank whose pool holds it
+ * and the byte offsets of its data and (FP8) its scale grid in that pool --
+ * the (memory region, offset) pair that addresses a one-sided write in
+ * "Weight transfer for RL post-training in under 2 seconds", section "RDMA
+ * WRITE: one-sided transfers". scale_off is 0 for a BF16 output. Errors:
+ * WT_ERR_INVALID_ARGUMENT (NULL argument, index out of range). */
 wt_status wt_plan_output_layout(const wt_plan* p, int32_t out, int32_t dst,
                                 int32_t* rank, uint64_t* data_off,
                                 uint64_t* scale_off);
@@ -221,7 +231,14 @@ wt_status wt_plan_shard_rows_read(const wt_plan* p, int32_t param, int32_t shard
 
 wt_status wt_plan_get_stats(const wt_plan* p, wt_plan_stats* stats);
 
-/* One step: run the preparation of every output on `stream`.
+/* One step: run the preparation of every output on `stream` -- the
+ * page's per-step work ("Weight transfer for RL post-training in under 2
+ * seconds", section "Task pipeline": rebuild each weight from its FSDP
+ * shards, fuse projections, quantize where the destination wants FP8),
+ * replaying the schedule compiled once by wt_plan_create (same page,
+ * sections "High-level workflow" and "Why it is fast and simple" / static
+ * schedule), with every write addressed by (pool, offset) as in its
+ * section "RDMA WRITE: one-sided transfers".
  * shard_ptrs: num_slots device pointers, param-major then shard (the order
  *   of wt_plan_desc.params and their shard_rows); each shard is a
  *   contiguous shard_rows x cols BF16 row-major block. A shard with 0 rows,
@@ -271,15 +288,35 @@ wt_status wt_prepare_offload(wt_plan* p, const void* host_image,
  * that loads the library holds it until the process exits), then runs the
  * same kernel as wt_prepare on the current device. Arguments and results
  * are those of wt_plan_create(desc) + wt_prepare(shard_ptrs, pools, stream).
- * The first call on a device looks up the array's device address there;
- * make that first call before any stream capture. Every call shares the
- * array, so calls whose work overlaps on the GPU (other streams, or other
- * threads) race: order them on one stream. Errors: as wt_plan_create and
- * wt_prepare; WT_ERR_INVALID_ARGUMENT when the tables need more than the
- * array's 4 MiB (roughly 120k 128x128 blocks), when offload_chunk_bytes is
- * set, or with WT_FLAG_DEBUG_CHECKS. Never calls cudaMalloc or cudaFree. */
+ * The first call on a device looks up the array's device address there.
+ * Every call shares the array, so calls whose work overlaps on the GPU
+ * (different streams) race: order them on one stream. Calls from several
+ * host threads onto one stream are safe: a library lock keeps each call's
+ * table upload and kernel adjacent. A wait that gives up inside the kernel
+ * is recorded outside the tables and kept until wt_noalloc_check reads it.
+ * Errors: as wt_plan_create and wt_prepare; WT_ERR_INVALID_ARGUMENT when
+ * the tables need more than the array's 4 MiB less 256 bytes (roughly 120k
+ * 128x128 blocks), when offload_chunk_bytes is set, with
+ * WT_FLAG_DEBUG_CHECKS, or when `stream` is being captured into a CUDA
+ * graph (the upload reads a host buffer that lives only for the call).
+ * Never calls cudaMalloc or cudaFree. */
 wt_status wt_prepare_noalloc(const wt_plan_desc* desc, const void* const* shard_ptrs,
                              void* const* pools, void* stream);
+
+/* The check of wt_prepare_noalloc, allocating nothing either: synchronise
+ * `stream`, then read and clear the error word that the kernels of earlier
+ * wt_prepare_noalloc calls on the current device share. WT_ERR_TIMEOUT if a
+ * wait inside one of them gave up (that step's pools are incomplete),
+ * WT_OK otherwise (also before any call on this device). No counterpart on
+ * the pages. Errors: WT_ERR_CUDA. */
+wt_status wt_noalloc_check(void* stream);
+
+/* Testing hook of wt_prepare_noalloc's bounded waits, like
+ * wt_debug_stall_unit for every later wt_prepare_noalloc call of the
+ * process: `unit` is never filled and every wait gives up after
+ * wait_limit_ns (0 = the default 2 s); unit = -1 restores normal
+ * operation. Errors: WT_ERR_INVALID_ARGUMENT (unit < -1). */
+wt_status wt_debug_noalloc_stall_unit(int64_t unit, uint64_t wait_limit_ns);
 
 /* The activation codec of the MoE dispatch: the same e4m3 arithmetic at
  * 1 x 128 granularity ("Enabling trillion-parameter models on AWS EFA",
@@ -365,10 +402,18 @@ wt_status wt_wait_counters(const uint32_t* counters, int32_t n, const uint32_t* 
 wt_status wt_debug_stall_unit(wt_plan* p, int64_t unit, uint64_t wait_limit_ns);
 
 /* Synchronise the plan's device with the last stream it ran on, then free
- * the plan and everything it owns. NULL is accepted. */
+ * the plan and everything it owns. NULL is accepted. The pages have no
+ * counterpart (their schedule lives as long as the training job). Errors:
+ * WT_ERR_CUDA if waiting for the last step failed (the plan is freed
+ * anyway). */
 wt_status wt_plan_destroy(wt_plan* p);
 
+/* Name of a status code ("WT_OK", "WT_ERR_SHAPE", ...); "WT_ERR_UNKNOWN"
+ * for a value outside the enum. A static string. No counterpart on the
+ * pages. */
 const char* wt_status_string(wt_status s);
+/* Detail of the calling thread's last failure (thread-local; valid until
+ * that thread's next failing call). No counterpart on the pages. */
 const char* wt_last_error(void);
 
 #ifdef __cplusplus

@@ -8,9 +8,8 @@ import torch
 import bf16_fp8_parameter_wt_b300 as wt
 from gpu_helpers import (CANARY, assert_pools_equal, device_pools, full_check, ncores,
                          oracle_pools, run_gpu)
-from workloads import (Output, Param, ValueRecipe, Workload, edge_stress, kimi_k2_moe_layer,
-                       llama_dense, llama_dense_tp4, make_shards, shards_to_host_u16, tiny_dense,
-                       tp_slices_small)
+from workloads import (Output, Param, ValueRecipe, Workload, edge_stress, llama_dense,
+                       llama_dense_tp4, make_shards, tiny_dense, tp_slices_small)
 
 pytestmark = pytest.mark.gpu
 
@@ -111,42 +110,6 @@ def test_pointer_tables_follow_new_buffers(oracle_mod):
         p.fill_(CANARY)
     run_gpu(w, shards2, pools=pools_a, plan=plan)
     assert_pools_equal(pools_a, want)
-    plan.close()
-
-
-def test_kimi_k2_layer_full_size_sampled(oracle_mod):
-    """The benchmark's workload at full size, in its launch configuration:
-    every output's scale grid is checked for range, and a seeded sample of
-    outputs (first, last = shared expert, and 14 others) byte for byte."""
-    w = kimi_k2_moe_layer()
-    shards = make_shards(w, device="cuda:0")
-    plan = wt.Plan(w, device=0)
-    pools = device_pools(plan, w.num_ranks)
-    run_gpu(w, shards, pools=pools, plan=plan)
-    rng = np.random.default_rng(2024)
-    sample = sorted({0, 1, len(w.outputs) - 2, len(w.outputs) - 1,
-                     *rng.choice(len(w.outputs), 12, replace=False).tolist()})
-    m = oracle_mod.Model(w)
-    for o in sample:
-        out = w.outputs[o]
-        flat = [None] * sum(len(p.shard_rows) for p in w.params)
-        base = np.cumsum([0] + [len(p.shard_rows) for p in w.params])
-        for q in out.parts:
-            for k, s in enumerate(shards[q]):
-                flat[base[q] + k] = shards_to_host_u16([[s]])[0]
-        data, scales = m.prepare_output(o, flat)
-        rank, doff, soff = plan.output_layout(o, 0)
-        got = pools[rank][doff:doff + data.size].cpu().numpy()
-        assert np.array_equal(got, data), out.name
-        gs = pools[rank][soff:soff + scales.size * 4].cpu().numpy().view(np.float32)
-        assert np.array_equal(gs.view(np.uint32), scales.view(np.uint32)), out.name
-    # every scale of every output is a positive finite amax/448 of N(0, 0.006) data
-    for o in range(len(w.outputs)):
-        rank, doff, soff = plan.output_layout(o, 0)
-        m_, n_ = w.output_shape(o)
-        k = (-(-m_ // 128)) * (-(-n_ // 128))
-        sc = pools[rank][soff:soff + 4 * k].view(torch.float32)
-        assert bool(torch.all((sc > 0.006 * 3 / 448) & (sc < 0.006 * 7 / 448)))
     plan.close()
 
 

@@ -107,3 +107,88 @@ def test_noalloc_runs_shard_local_plans(halo):
         for r in range(w.num_ranks):
             assert torch.equal(got[r], want[r]), (s, r)
         plan.close()
+
+
+def test_noalloc_reports_a_wait_that_gave_up_then_recovers():
+    """A kernel wait that runs out (one unit's stage left unfilled on the
+    host's request, 50 ms wait limit) is kept outside the uploaded tables and
+    reported by wt_noalloc_check, even after a later call; the check clears
+    it and the next step is complete again."""
+    w = tiny_dense()
+    shards = make_shards(w, device="cuda:0")
+    flat = [s.data_ptr() for per in shards for s in per]
+    stream = torch.cuda.current_stream().cuda_stream
+    plan = wt.Plan(w, device=0)
+    want = _pools(plan, w.num_ranks, CANARY)
+    plan.prepare(flat, [p.data_ptr() for p in want], stream)
+    desc = wt.PlanDesc(w)
+    got = _pools(plan, w.num_ranks, CANARY)
+    wt.wt_noalloc_check(stream)                  # nothing recorded before
+    try:
+        wt.wt_debug_noalloc_stall_unit(3, 50_000_000)
+        wt.wt_prepare_noalloc(desc, flat, [p.data_ptr() for p in got], stream)
+    finally:
+        wt.wt_debug_noalloc_stall_unit(-1, 0)
+    # a second, normal call in between does not wipe the record
+    wt.wt_prepare_noalloc(desc, flat, [p.data_ptr() for p in got], stream)
+    with pytest.raises(wt.WTError) as ei:
+        wt.wt_noalloc_check(stream)
+    assert ei.value.name == "WT_ERR_TIMEOUT"
+    wt.wt_noalloc_check(stream)                  # cleared by the report
+    for p in got:
+        p.fill_(CANARY)
+    wt.wt_prepare_noalloc(desc, flat, [p.data_ptr() for p in got], stream)
+    wt.wt_noalloc_check(stream)
+    for r in range(w.num_ranks):
+        assert torch.equal(got[r], want[r]), r
+    plan.close()
+
+
+def test_noalloc_refuses_stream_capture():
+    """The call uploads a host image that lives only for the call, so a
+    captured copy would read freed memory at replay: it is refused."""
+    w = tiny_dense()
+    shards = make_shards(w, device="cuda:0")
+    flat = [s.data_ptr() for per in shards for s in per]
+    plan = wt.Plan(w, device=0, pool_capacity=None)
+    pools = _pools(plan, w.num_ranks, CANARY)
+    plan.close()
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):
+        wt.wt_prepare_noalloc(wt.PlanDesc(w), flat, [p.data_ptr() for p in pools], stream.cuda_stream)
+    stream.synchronize()
+    with pytest.raises(wt.WTError) as ei:
+        with torch.cuda.graph(torch.cuda.CUDAGraph(), stream=stream):
+            pools[0].add_(0)
+            wt.wt_prepare_noalloc(wt.PlanDesc(w), flat, [p.data_ptr() for p in pools],
+                                  stream.cuda_stream)
+    assert ei.value.name == "WT_ERR_INVALID_ARGUMENT"
+    assert "captured" in str(ei.value)
+    torch.cuda.synchronize()
+
+
+def test_noalloc_takes_no_device_memory():
+    """After a first call on the device (which loads the library's module
+    and its fixed array), further calls -- including a larger schedule --
+    leave the device's free memory unchanged: nothing is allocated."""
+    ws = [tiny_dense(), kimi_k2_moe_layer(40)]
+    bufs = []
+    for w in ws:
+        shards = make_shards(w, device="cuda:0")
+        flat = [s.data_ptr() for per in shards for s in per]
+        plan = wt.Plan(w, device=-1)
+        pools = _pools(plan, w.num_ranks, CANARY)
+        plan.close()
+        bufs.append((w, shards, flat, pools, wt.PlanDesc(w)))
+    stream = torch.cuda.current_stream().cuda_stream
+    w, _, flat, pools, desc = bufs[0]
+    wt.wt_prepare_noalloc(desc, flat, [p.data_ptr() for p in pools], stream)
+    wt.wt_noalloc_check(stream)
+    torch.cuda.synchronize()
+    free0 = torch.cuda.mem_get_info(0)[0]
+    for _ in range(3):
+        for w, _, flat, pools, desc in reversed(bufs):
+            wt.wt_prepare_noalloc(desc, flat, [p.data_ptr() for p in pools], stream)
+        wt.wt_noalloc_check(stream)
+    torch.cuda.synchronize()
+    assert torch.cuda.mem_get_info(0)[0] == free0
