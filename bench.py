@@ -17,12 +17,16 @@ inside the timed region. `--workload offload_8layer` instead times the
 8-layer streamed-offload stack (its own JSON line). `--impl reference` times the CPU
 oracle on the host cores on a bounded sample of the same workload.
 Under torchrun each rank prepares its own layer (weak scaling, no
-collective on the data path). With --shard-local the ranks instead share
-one layer as an FSDP group of --fsdp ranks (default: the world size): rank
-r holds only shard r of every weight and prepares the blocks of its own
-rows with a shard-local plan, no exchange (strong scaling; `value` counts
-the bytes of all ranks). At one GPU, --shard-local --fsdp 8 times what one
-rank of an 8-way group does.
+collective on the data path). With --partition sources the ranks share one
+layer and each prepares the outputs that schedule.assign_sources gives it
+(strong scaling; --sources 8 at one GPU times rank 0's share). With
+--shard-local the ranks instead share one layer as an FSDP group of --fsdp
+ranks (default: the world size): rank r holds only shard r of every weight
+and prepares the blocks of its own rows with a shard-local plan (strong
+scaling; `value` counts the bytes of all ranks); with --halo the halo rows
+are exchanged point to point inside every timed step, and `exchange_ms` is
+that exchange's share of the step. At one GPU, --shard-local --fsdp 8 times
+what one rank of an 8-way group does.
 """
 from __future__ import annotations
 
@@ -195,6 +199,51 @@ def sum_over_ranks(world, v: float, dev) -> float:
     return float(t.item())
 
 
+def rank_work(workload, partition: str, world: int, rank: int, fsdp: int = 0,
+              halo: bool = False, experts: int = 385, sources: int = 0):
+    """What one rank prepares: (workload, Plan keyword arguments, note).
+      replicas    : a model of its own (the MoE layer drawn with a per-rank
+                    seed; other workloads as they are), the full plan --
+                    weak scaling, no exchange;
+      sources     : one model shared by every rank (same seeds), and the
+                    outputs that assign_sources gives rank `rank` of
+                    `sources` source GPUs (default: the world size) --
+                    strong scaling, no exchange on the data path;
+      shard-local : one model shared by an FSDP group of `fsdp` ranks
+                    (default: the world size), sharded `fsdp` ways, and rank
+                    r's shard-local plan (halo: boundaries off the 128-row
+                    grid, halo rows received from the next ranks) -- strong
+                    scaling.
+    `workload` is a name, or a workload object shared as it is."""
+    from bf16_fp8_parameter_wt_b300.schedule import rank_view
+    from workloads import WORKLOADS, kimi_k2_moe_layer
+    moe = workload == "kimi_k2_moe_layer"
+    if not isinstance(workload, str):
+        model = workload
+        workload = model.name
+        WORKLOADS = {workload: lambda: model}
+    if partition == "replicas":
+        w = kimi_k2_moe_layer(experts, seed=1003 + rank) if moe else WORKLOADS[workload]()
+        return w, {}, f"replicas x{world}" if world > 1 else "single"
+    if partition == "sources":
+        n = sources or world
+        if not 0 <= rank < n:
+            raise ValueError(f"rank {rank} has no share among {n} sources")
+        w = kimi_k2_moe_layer(experts) if moe else WORKLOADS[workload]()
+        sub, mine = rank_view(w, n, rank)
+        return sub, {}, f"source {rank} of {n} ({len(mine)} of {len(w.outputs)} outputs by assign_sources)"
+    if partition == "shard-local":
+        f = fsdp or world
+        if not 0 <= rank < f:
+            raise ValueError(f"rank {rank} is outside an FSDP group of {f}")
+        w = kimi_k2_moe_layer(experts, shards=f) if moe else WORKLOADS[workload]()
+        if any(len(p.shard_rows) != f for p in w.params):
+            raise ValueError(f"{w.name} has {len(w.params[0].shard_rows)} shards per weight: use that FSDP degree")
+        note = f"shard-local rank {rank} of an FSDP group of {f}" + (" with halos" if halo else "")
+        return w, {"local_shard": rank, "halo": halo}, note
+    raise ValueError(partition)
+
+
 def sample_outputs(w, experts: int, target_bytes: int = 700_000_000) -> list:
     """A bounded sample of a workload's outputs: the first `experts` experts
     of an MoE layer, else the outputs in plan order up to about
@@ -325,6 +374,12 @@ def main():
     ap.add_argument("--fsdp", type=int, default=0, help="FSDP degree for --shard-local (0: world)")
     ap.add_argument("--halo", action="store_true",
                     help="with --shard-local: shard boundaries off the 128-row grid, halo rows exchanged")
+    ap.add_argument("--partition", default="replicas", choices=["replicas", "sources"],
+                    help="under torchrun: a layer per rank (replicas) or one layer split over "
+                         "the ranks by assign_sources (sources)")
+    ap.add_argument("--sources", type=int, default=0,
+                    help="with --partition sources: number of source GPUs (0: world size); "
+                         "at one GPU, --sources 8 times rank 0's share")
     ap.add_argument("--counters", choices=["launch", "block"], default=None,
                     help="time the step with per-rank completion counters")
     ap.add_argument("--tokens", type=int, default=131072)
@@ -356,40 +411,41 @@ def main():
     wt_build.build()
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    fsdp = (args.fsdp or world) if args.shard_local else 0
-    if args.halo and not args.shard_local:
+    partition = "shard-local" if args.shard_local else args.partition
+    if args.halo and partition != "shard-local":
         ap.error("--halo needs --shard-local")
-    if args.shard_local:
-        # one model shared by the group: every rank draws the same values
-        if args.workload == "kimi_k2_moe_layer":
-            w = kimi_k2_moe_layer(args.experts, shards=fsdp)
-        elif args.workload in ("offload_8layer", "tokens"):
-            ap.error("--shard-local prepares a plan workload")
-        else:
-            w = WORKLOADS[args.workload]()
-            if any(len(p.shard_rows) != fsdp for p in w.params):
-                ap.error(f"{w.name} has {len(w.params[0].shard_rows)} shards per weight: use that --fsdp")
-        if rank >= fsdp:
-            ap.error("--fsdp must be at least the world size")
-    elif args.workload == "kimi_k2_moe_layer":
-        w = kimi_k2_moe_layer(args.experts, seed=1003 + rank)
-    else:
-        w = WORKLOADS[args.workload]()
-    plan = wt.Plan(w, device=local, local_shard=rank if args.shard_local else -1, halo=args.halo)
+    if partition != "replicas" and args.workload in ("offload_8layer", "tokens"):
+        ap.error(f"--partition {partition} prepares a plan workload")
+    fsdp = (args.fsdp or world) if partition == "shard-local" else 0
+    try:
+        w, plan_kw, parallelism = rank_work(args.workload, partition, world, rank, fsdp=fsdp,
+                                            halo=args.halo, experts=args.experts, sources=args.sources)
+    except ValueError as e:
+        ap.error(str(e))
+    plan = wt.Plan(w, device=local, **plan_kw)
     shards = make_shards(w, device=dev)
     halo_bytes = 0
-    if args.shard_local:
+    exchange = None            # the per-step halo exchange under torchrun
+    if partition == "shard-local":
         # this rank keeps its own shard of every weight, plus the halo rows
-        # its plan reads from other shards: received from their ranks under
-        # torchrun, cut from the locally drawn copy at one GPU
+        # its plan reads from other shards: received from their ranks into
+        # fixed buffers under torchrun (every timed step exchanges them
+        # again), cut from the locally drawn copy at one GPU
         need = {(i, k): plan.shard_rows_read(i, k) for i, per in enumerate(shards)
                 for k in range(len(per)) if k != rank}
         if world > 1 and args.halo:
             if fsdp != world:
                 ap.error("exchanging halos needs --fsdp equal to the world size")
-            from bf16_fp8_parameter_wt_b300.schedule import exchange_halos, halo_transfers
+            from bf16_fp8_parameter_wt_b300.schedule import exchange_halos, halo_buffers, halo_transfers
+            transfers = halo_transfers(w, fsdp)
+            got = halo_buffers(w, transfers, rank, dev)
+            own = [per[rank] for per in shards]
             barrier(world)                     # a collective before the first point-to-point batch
-            got = exchange_halos(w, halo_transfers(w, fsdp), rank, [per[rank] for per in shards])
+
+            def exchange():
+                exchange_halos(w, transfers, rank, own, out=got)
+
+            exchange()
         else:
             got = {key: shards[key[0]][key[1]][:n].clone() for key, n in need.items() if n}
         shards = [[s if k == rank else got.get((i, k), s.new_empty(0)) for k, s in enumerate(per)]
@@ -418,26 +474,37 @@ def main():
     first_step_host_ms = (time.perf_counter() - t_first) * 1e3
     with torch.cuda.stream(stream):
         for _ in range(args.warmup - 1):
+            if exchange:
+                exchange()
             plan.prepare(shard_ptrs, pool_ptrs, sp)
     stream.synchronize()
 
     bus = gpu_bus_id(dev)
+    # a step is [halo exchange (torchrun, --halo)] + wt_prepare; the launch's
+    # own time runs from `mids` to `ends`
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    mids = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)] if exchange else starts
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     barrier(world)
     torch.cuda.synchronize(dev)
     clocks = ClockSampler(bus)
     time.sleep(0.3)
     t_wall = time.perf_counter()
-    for i in range(args.steps):
-        starts[i].record(stream)
-        plan.prepare(shard_ptrs, pool_ptrs, sp)
-        ends[i].record(stream)
+    with torch.cuda.stream(stream):
+        for i in range(args.steps):
+            starts[i].record(stream)
+            if exchange:
+                exchange()             # NCCL point-to-point; its completion is ordered on `stream`
+                mids[i].record(stream)
+            plan.prepare(shard_ptrs, pool_ptrs, sp)
+            ends[i].record(stream)
     stream.synchronize()
     t_wall = time.perf_counter() - t_wall
     barrier(world)
     clk = clocks.stop()
-    per_launch_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    per_launch_ms = [s.elapsed_time(e) for s, e in zip(mids, ends)]
+    exchange_ms = (round(statistics.mean(s.elapsed_time(m) for s, m in zip(starts, mids)), 4)
+                   if exchange else None)
     total_ms = starts[0].elapsed_time(ends[-1])
     total_ms = max_over_ranks(world, total_ms, dev)
     ms_per_step = total_ms / args.steps
@@ -454,7 +521,7 @@ def main():
     achieved = alg_bytes / avg_launch_s / 1e9
     traffic = (TRAFFIC["bytes_per_launch"]
                if TRAFFIC["kernel_sha256"] == kernel_sha() and args.workload == "kimi_k2_moe_layer"
-               and TRAFFIC["experts"] == args.experts and not args.shard_local else None)
+               and TRAFFIC["experts"] == args.experts and partition == "replicas" else None)
     roofline = {"bound": "hbm", "achieved": round(achieved, 1),
                 "peak": peak if peak else 6400.0, "unit": "GB/s",
                 "frac": round(achieved / (peak if peak else 6400.0), 4),
@@ -491,14 +558,14 @@ def main():
         graph_us = round(g0.elapsed_time(g1) * 1e3 / 20, 2)
 
     e2e = None
-    if args.shard_local:
+    if partition == "shard-local":
         e2e = {"value": None, "reason": "shard-local plans do not stage offloaded shards"}
     elif not args.no_e2e:
         del pools
         torch.cuda.empty_cache()
         e2e = measure_e2e(w, shards, args, dev, world)
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline and not args.shard_local:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and partition == "replicas":
         del shards, flat
         torch.cuda.empty_cache()
         cpu = cpu_baseline(w, args.cpu_experts)
@@ -506,7 +573,7 @@ def main():
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
-        "higher_is_better": True, "scaling": "strong" if args.shard_local else "weak",
+        "higher_is_better": True, "scaling": "weak" if partition == "replicas" else "strong",
         "vs_baseline": None, "dtype": "f32",
         "data": f"synthetic (seeded {w.values.dist}, sigma {w.values.sigma}, BF16, generated on device)",
         "params_per_s": round(params_per_s, 1),
@@ -517,9 +584,9 @@ def main():
                    "l2": (f"inputs ({st['bytes_read'] / 1e9:.1f} GB) larger than the 126 MB L2, no flush"
                           if st["bytes_read"] > L2_BYTES else
                           "inputs smaller than L2: L2-resident, a latency figure"),
-                   "halo_bytes_per_rank": halo_bytes if args.shard_local else None,
-                   "parallelism": (f"shard-local rank {rank} of an FSDP group of {fsdp}" if args.shard_local
-                                   else f"replicas x{world}" if world > 1 else "single")},
+                   "halo_bytes_per_rank": halo_bytes if partition == "shard-local" else None,
+                   "parallelism": parallelism},
+        "exchange_ms": exchange_ms,
         "roofline": roofline, "graph_replay_us": graph_us,
         "first_step_host_ms": round(first_step_host_ms, 2), "shards": st["num_slots"],
         "completion_counters": args.counters,

@@ -53,19 +53,22 @@ void free_device(Plan& p) {
   if (p.device < 0) return;
   DeviceGuard g(p.device);
   if (p.d_tables) cudaFree(p.d_tables);
-  if (p.h_pinned) cudaFreeHost(p.h_pinned);
+  for (PtrSet& ps : p.sets) {
+    if (ps.h_pinned) cudaFreeHost(ps.h_pinned);
+    if (ps.upload_done) cudaEventDestroy(ps.upload_done);
+    ps.h_pinned = nullptr;
+    ps.upload_done = nullptr;
+  }
   for (int b = 0; b < 2; ++b) {
     if (p.staging[b]) cudaFree(p.staging[b]);
     if (p.h2d_done[b]) cudaEventDestroy(p.h2d_done[b]);
     if (p.prep_done[b]) cudaEventDestroy(p.prep_done[b]);
   }
-  if (p.ptr_upload_done) cudaEventDestroy(p.ptr_upload_done);
   if (p.last_done) cudaEventDestroy(p.last_done);
   p.d_tables = nullptr;
-  p.h_pinned = nullptr;
 }
 
-// Layout of the dynamic pointer block (identical on the device and in the
+// Layout of a pointer-table block (identical on the device and in its
 // pinned staging buffer): shard pointers, their tensor maps, destinations.
 struct DynLayout {
   size_t shards = 0, tmaps = 0, dsts = 0, bytes = 0;
@@ -107,7 +110,7 @@ wt_status upload(Plan& p, int device) {
   const DynLayout dl = dyn_layout(p);
   size_t off = 0;
   auto take = [&](size_t bytes) { size_t o = off; off = align256(off + bytes); return o; };
-  const size_t o_dyn = take(dl.bytes);
+  const size_t o_dyn = take(dl.bytes * kPtrSets);
   const size_t o_units = take(p.h_units.size() * sizeof(DevUnit));
   const size_t o_runs = take(p.h_runs.size() * sizeof(DevRun));
   const size_t o_geom = take(p.h_geom.size() * sizeof(DevDstGeom));
@@ -123,6 +126,7 @@ wt_status upload(Plan& p, int device) {
             (uint32_t)(((ds.rows + kTile - 1) / kTile) * ((ds.cols + kTile - 1) / kTile));
   const size_t o_lc = take(lc.size() * sizeof(uint32_t));
   const size_t o_err = take(sizeof(int32_t));
+  const size_t o_ticket = take(2 * sizeof(uint32_t));
   const size_t o_offl_s = take(offload ? n_slots * sizeof(void*) : 0);
   const size_t o_offl_t = take(offload ? n_slots * kTmapBytes : 0);
   e = cudaMalloc(&p.d_tables, std::max<size_t>(off, 256));
@@ -131,23 +135,21 @@ wt_status upload(Plan& p, int device) {
   auto put = [&](size_t o, const void* src, size_t bytes) {
     return bytes ? cudaMemcpy(base + o, src, bytes, cudaMemcpyHostToDevice) : cudaSuccess;
   };
-  if ((e = cudaMemset(base + o_dyn, 0, dl.bytes)) != cudaSuccess ||
+  if ((e = cudaMemset(base + o_dyn, 0, dl.bytes * kPtrSets)) != cudaSuccess ||
       (e = put(o_units, p.h_units.data(), p.h_units.size() * sizeof(DevUnit))) != cudaSuccess ||
       (e = put(o_runs, p.h_runs.data(), p.h_runs.size() * sizeof(DevRun))) != cudaSuccess ||
       (e = put(o_geom, p.h_geom.data(), p.h_geom.size() * sizeof(DevDstGeom))) != cudaSuccess ||
       (e = put(o_bmap, p.h_blockmap.data(), p.h_blockmap.size() * sizeof(int32_t))) != cudaSuccess ||
       (e = put(o_drank, p.h_dst_rank.data(), p.h_dst_rank.size() * sizeof(int32_t))) != cudaSuccess ||
       (e = put(o_lc, lc.data(), lc.size() * sizeof(uint32_t))) != cudaSuccess ||
-      (e = cudaMemset(base + o_err, 0, sizeof(int32_t))) != cudaSuccess)
+      (e = cudaMemset(base + o_err, 0, sizeof(int32_t))) != cudaSuccess ||
+      (e = cudaMemset(base + o_ticket, 0, 2 * sizeof(uint32_t))) != cudaSuccess)
     return cuda_fail(e, "uploading plan tables");
   p.dyn_bytes = dl.bytes;
-  p.d_shard_ptrs = reinterpret_cast<const uint16_t**>(base + o_dyn + dl.shards);
-  p.d_tmaps = reinterpret_cast<unsigned char*>(base + o_dyn + dl.tmaps);
-  p.d_dst_ptrs = reinterpret_cast<DevDstPtr*>(base + o_dyn + dl.dsts);
   p.d_error = reinterpret_cast<int32_t*>(base + o_err);
   p.args.units = reinterpret_cast<const DevUnit*>(base + o_units);
   p.args.runs = reinterpret_cast<const DevRun*>(base + o_runs);
-  p.args.dst_ptrs = p.d_dst_ptrs;
+  p.args.ticket = reinterpret_cast<uint32_t*>(base + o_ticket);
   p.args.geom = reinterpret_cast<const DevDstGeom*>(base + o_geom);
   p.args.dst_rank = reinterpret_cast<const int32_t*>(base + o_drank);
   p.d_launch_counts = reinterpret_cast<uint32_t*>(base + o_lc);
@@ -155,15 +157,19 @@ wt_status upload(Plan& p, int device) {
   p.args.error_word = p.d_error;
   p.args.timeout_ns = kDefaultTimeoutNs;
 
-  e = cudaHostAlloc(&p.h_pinned, std::max<size_t>(dl.bytes, 256), cudaHostAllocDefault);
-  if (e != cudaSuccess) return alloc_fail("pinned pointer staging allocation failed");
-  std::memset(p.h_pinned, 0, std::max<size_t>(dl.bytes, 256));
-  if ((e = cudaEventCreateWithFlags(&p.ptr_upload_done, cudaEventDisableTiming)) != cudaSuccess ||
-      (e = cudaEventCreateWithFlags(&p.last_done, cudaEventDisableTiming)) != cudaSuccess)
+  for (int j = 0; j < kPtrSets; ++j) {
+    PtrSet& ps = p.sets[j];
+    ps.d_block = reinterpret_cast<unsigned char*>(base + o_dyn + (size_t)j * dl.bytes);
+    e = cudaHostAlloc(&ps.h_pinned, std::max<size_t>(dl.bytes, 256), cudaHostAllocDefault);
+    if (e != cudaSuccess) return alloc_fail("pinned pointer staging allocation failed");
+    std::memset(ps.h_pinned, 0, std::max<size_t>(dl.bytes, 256));
+    if ((e = cudaEventCreateWithFlags(&ps.upload_done, cudaEventDisableTiming)) != cudaSuccess)
+      return cuda_fail(e, "cudaEventCreate");
+    ps.shards.assign(n_slots, nullptr);
+    ps.pools.assign((size_t)p.num_ranks, nullptr);
+  }
+  if ((e = cudaEventCreateWithFlags(&p.last_done, cudaEventDisableTiming)) != cudaSuccess)
     return cuda_fail(e, "cudaEventCreate");
-  p.cached_shards.assign(n_slots, nullptr);
-  p.cached_pools.assign((size_t)p.num_ranks, nullptr);
-  p.shards_valid = p.pools_valid = false;
 
   if (offload) {
     // the watermark: two staging buffers of the largest chunk
@@ -203,22 +209,46 @@ wt_status upload(Plan& p, int device) {
   return WT_OK;
 }
 
-// Check the caller's pointers and, when they changed since the last call,
-// rebuild the dynamic pointer block (shard pointers, the shards' tensor
-// maps, absolute destination addresses) on the host and queue one copy on s.
+// Check the caller's pointers and find the pointer-table set that holds
+// them; when none does, rebuild the least recently used set on the host
+// (shard pointers, the shards' tensor maps, absolute destination addresses,
+// each part only if it changed) and queue one copy of it on s. shards ==
+// NULL (offload): only the destinations matter. The only host wait is for
+// the earlier upload from the replaced set's staging buffer, kPtrSets
+// uploads back.
 wt_status stage_pointers(Plan& p, const void* const* shards, void* const* pools, cudaStream_t s,
-                         bool capturing) {
+                         bool capturing, int* set_out) {
   const size_t n_slots = (size_t)p.num_slots, n_ranks = (size_t)p.num_ranks;
-  const bool shards_changed =
-      shards && !(p.shards_valid && std::equal(p.cached_shards.begin(), p.cached_shards.end(), shards));
-  const bool pools_changed =
-      !(p.pools_valid && std::equal(p.cached_pools.begin(), p.cached_pools.end(), pools));
-  if (!shards_changed && !pools_changed) return WT_OK;
+  auto same_shards = [&](const PtrSet& ps) {
+    return ps.shards_valid && std::equal(ps.shards.begin(), ps.shards.end(), shards);
+  };
+  auto same_pools = [&](const PtrSet& ps) {
+    return ps.pools_valid && std::equal(ps.pools.begin(), ps.pools.end(), pools);
+  };
+  for (int j = 0; j < kPtrSets; ++j) {
+    PtrSet& ps = p.sets[j];
+    if (same_pools(ps) && (!shards || same_shards(ps))) {
+      ps.last_use = ++p.use_clock;
+      // a graph replays this set's addresses: it must stay as it is
+      if (capturing) ps.captured = true;
+      *set_out = j;
+      return WT_OK;
+    }
+  }
   // a captured copy would read the staging buffer at every replay, after
   // later calls may have rewritten it
   if (capturing)
     return fail(WT_ERR_INVALID_ARGUMENT,
                 "new shard or pool pointers inside a stream capture: stage them with an uncaptured call first");
+  int victim = -1;
+  for (int j = 0; j < kPtrSets; ++j)
+    if (!p.sets[j].captured && (victim < 0 || p.sets[j].last_use < p.sets[victim].last_use)) victim = j;
+  if (victim < 0)
+    return fail(WT_ERR_INVALID_ARGUMENT,
+                "every pointer-table set holds addresses that a captured CUDA graph replays");
+  PtrSet& ps = p.sets[victim];
+  const bool shards_changed = shards && !same_shards(ps);
+  const bool pools_changed = !same_pools(ps);
   if (pools_changed)
     for (size_t r = 0; r < n_ranks; ++r) {
       if (p.pool_bytes[r] == 0) continue;
@@ -237,21 +267,20 @@ wt_status stage_pointers(Plan& p, const void* const* shards, void* const* pools,
           return fail(WT_ERR_ALIGNMENT, pi.name + ": shard " + std::to_string(k) + " is misaligned");
       }
     }
-  // the pinned staging may still be read by the previous upload
-  cudaError_t e = cudaEventSynchronize(p.ptr_upload_done);
-  if (e != cudaSuccess) return cuda_fail(e, "waiting for the previous pointer upload");
+  // the staging buffer may still be read by this set's previous upload
+  cudaError_t e = ps.uploaded ? cudaEventSynchronize(ps.upload_done) : cudaSuccess;
+  if (e != cudaSuccess) return cuda_fail(e, "waiting for an earlier pointer upload");
   const DynLayout dl = dyn_layout(p);
-  char* h = static_cast<char*>(p.h_pinned);
+  char* h = static_cast<char*>(ps.h_pinned);
   if (shards_changed) {
+    ps.shards_valid = false;
     std::memcpy(h + dl.shards, shards, n_slots * sizeof(void*));
     wt_status st = encode_tmaps(p, shards, reinterpret_cast<unsigned char*>(h + dl.tmaps));
-    if (st != WT_OK) {
-      p.shards_valid = false;
-      return st;
-    }
-    p.tmaps_dirty = true;
+    if (st != WT_OK) return st;
+    ps.tmaps_dirty = true;
   }
   if (pools_changed) {
+    ps.pools_valid = false;
     DevDstPtr* dp = reinterpret_cast<DevDstPtr*>(h + dl.dsts);
     for (const OutputInfo& oi : p.outputs)
       for (size_t k = 0; k < oi.dsts.size(); ++k) {
@@ -264,16 +293,27 @@ wt_status stage_pointers(Plan& p, const void* const* shards, void* const* pools,
         d.pool_end = pool + p.pool_bytes[ds.rank];
       }
   }
-  e = cudaMemcpyAsync(p.d_shard_ptrs, h, dl.bytes, cudaMemcpyHostToDevice, s);
+  e = cudaMemcpyAsync(ps.d_block, h, dl.bytes, cudaMemcpyHostToDevice, s);
   if (e != cudaSuccess) return cuda_fail(e, "pointer table upload");
-  if ((e = cudaEventRecord(p.ptr_upload_done, s)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
+  if ((e = cudaEventRecord(ps.upload_done, s)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
+  ps.uploaded = true;
   if (shards_changed) {
-    std::copy(shards, shards + n_slots, p.cached_shards.begin());
-    p.shards_valid = true;
+    std::copy(shards, shards + n_slots, ps.shards.begin());
+    ps.shards_valid = true;
   }
-  std::copy(pools, pools + n_ranks, p.cached_pools.begin());
-  p.pools_valid = true;
+  std::copy(pools, pools + n_ranks, ps.pools.begin());
+  ps.pools_valid = true;
+  ps.last_use = ++p.use_clock;
+  *set_out = victim;
   return WT_OK;
+}
+
+// The kernel's view of one pointer-table set.
+void bind_set(const Plan& p, const PtrSet& ps, PrepArgs& a) {
+  const DynLayout dl = dyn_layout(p);
+  a.shard_ptrs = reinterpret_cast<const uint16_t* const*>(ps.d_block + dl.shards);
+  a.tmaps = ps.d_block + dl.tmaps;
+  a.dst_ptrs = reinterpret_cast<const DevDstPtr*>(ps.d_block + dl.dsts);
 }
 
 // One persistent CTA per SM (each holds a 128 KiB shared-memory ring).
@@ -378,14 +418,15 @@ wt_status wt_prepare(wt_plan* h, const void* const* shard_ptrs, void* const* poo
   cudaError_t e = cudaStreamIsCapturing(s, &cap);
   if (e != cudaSuccess) return cuda_fail(e, "cudaStreamIsCapturing");
   const bool capturing = cap != cudaStreamCaptureStatusNone;
-  wt_status st = stage_pointers(p, shard_ptrs, pools, s, capturing);
+  int set = 0;
+  wt_status st = stage_pointers(p, shard_ptrs, pools, s, capturing, &set);
   if (st != WT_OK) return st;
+  PtrSet& ps = p.sets[set];
   PrepArgs a = p.args;
-  a.shard_ptrs = p.d_shard_ptrs;
-  a.tmaps = p.d_tmaps;
+  bind_set(p, ps, a);
   a.stall_unit = p.stall_unit;
   a.timeout_ns = p.wait_limit_ns ? p.wait_limit_ns : kDefaultTimeoutNs;
-  a.tmap_fence = p.tmaps_dirty ? 1u : 0u;
+  a.tmap_fence = ps.tmaps_dirty ? 1u : 0u;
   a.counters = p.count_mode == WT_COUNT_PER_BLOCK ? p.counters : nullptr;
   a.unit_begin = 0;
   a.unit_end = p.num_units;
@@ -395,7 +436,7 @@ wt_status wt_prepare(wt_plan* h, const void* const* shard_ptrs, void* const* poo
       (e = launch_add_counts(p.counters, p.d_launch_counts, p.num_ranks, p.d_error, s)) != cudaSuccess)
     return cuda_fail(e, "completion count launch");
   if (capturing) return WT_OK;         // the graph's replays are the caller's to track
-  p.tmaps_dirty = false;
+  ps.tmaps_dirty = false;
   if ((e = cudaEventRecord(p.last_done, s)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
   p.ran = true;
   return WT_OK;
@@ -418,9 +459,11 @@ wt_status wt_prepare_offload(wt_plan* h, const void* host_image, void* const* po
   if (cudaStreamIsCapturing(ks, &cap) != cudaSuccess || cap != cudaStreamCaptureStatusNone ||
       cudaStreamIsCapturing(cs, &cap) != cudaSuccess || cap != cudaStreamCaptureStatusNone)
     return fail(WT_ERR_INVALID_ARGUMENT, "wt_prepare_offload cannot be captured into a CUDA graph");
-  wt_status st = stage_pointers(p, nullptr, pools, ks, false);
+  int set = 0;
+  wt_status st = stage_pointers(p, nullptr, pools, ks, false, &set);
   if (st != WT_OK) return st;
   PrepArgs a = p.args;
+  bind_set(p, p.sets[set], a);
   a.shard_ptrs = p.d_offload_shard_ptrs;
   a.tmaps = p.d_offload_tmaps;
   a.counters = p.count_mode == WT_COUNT_PER_BLOCK ? p.counters : nullptr;

@@ -94,7 +94,8 @@ extern "C" wt_status wt_prepare_noalloc(const wt_plan_desc* desc, const void* co
   if (st != WT_OK) return st;
 
   // table image: shard pointers, their tensor maps, destinations, unit
-  // descriptors, row runs, destination geometry and block maps
+  // descriptors, row runs, destination geometry and block maps, and the
+  // kernel's ticket counter (zero, like every launch needs it)
   const size_t n_slots = (size_t)p.num_slots;
   const size_t o_shards = 0;
   const size_t o_tmaps = up256(o_shards + n_slots * sizeof(void*));
@@ -103,7 +104,8 @@ extern "C" wt_status wt_prepare_noalloc(const wt_plan_desc* desc, const void* co
   const size_t o_runs = up256(o_units + p.h_units.size() * sizeof(DevUnit));
   const size_t o_geom = up256(o_runs + p.h_runs.size() * sizeof(DevRun));
   const size_t o_bmap = up256(o_geom + p.h_geom.size() * sizeof(DevDstGeom));
-  const size_t total = up256(o_bmap + p.h_blockmap.size() * sizeof(int32_t));
+  const size_t o_ticket = up256(o_bmap + p.h_blockmap.size() * sizeof(int32_t));
+  const size_t total = o_ticket + 256;
   if (total > kErrorOffset)
     return fail_na(WT_ERR_INVALID_ARGUMENT,
                    "schedule tables need " + std::to_string(total) +
@@ -182,6 +184,7 @@ extern "C" wt_status wt_prepare_noalloc(const wt_plan_desc* desc, const void* co
   a.unit_begin = 0;
   a.unit_end = p.num_units;
   a.error_word = reinterpret_cast<int32_t*>(dbase + kErrorOffset);
+  a.ticket = reinterpret_cast<uint32_t*>(dbase + o_ticket);
   const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(p.num_units, g_sm_count[device]));
   e = launch_prepare(a, grid, s, false);
   if (e != cudaSuccess) return fail_na(WT_ERR_CUDA, std::string("preparation kernel launch: ") + cudaGetErrorString(e));

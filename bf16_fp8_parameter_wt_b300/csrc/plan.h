@@ -22,6 +22,7 @@ constexpr uint32_t kUnitFp8 = 1u;    // e4m3 codes + scale, else BF16 bytes
 constexpr uint32_t kUnitVec = 2u;    // rows are 16-byte aligned: bulk-copy path, else element path
 constexpr uint32_t kUnitMulti = 4u;  // block rows come from more than one shard
 constexpr uint32_t kUnitSliced = 8u; // some destination of the output takes a slice
+constexpr uint32_t kUnitEnd = 0x80u; // in the kernel only: a stage that ends the CTA's units
 
 // Error word bits set by the kernel
 constexpr int32_t kErrBadStore = 1;  // debug checks: a store fell outside its pool range
@@ -92,6 +93,10 @@ struct PrepArgs {
   uint64_t timeout_ns;               // limit of every wait inside the kernel
   uint32_t tmap_fence;               // tensor maps were rewritten since the last launch
   int64_t stall_unit;                // testing: this unit is never filled (-1: none)
+  // Two words, zero before a launch and reset to zero by its last CTA: the
+  // next ticket (a batch of kBatch consecutive units) and the CTAs done.
+  // NULL: units are assigned statically (CTA b takes b, b + grid, ...).
+  uint32_t* ticket;
 };
 
 // Host-side copy of one param.
@@ -131,6 +136,26 @@ struct Chunk {
   uint64_t host_begin = 0, host_bytes = 0;
 };
 
+// One set of the caller's buffer addresses as the kernel reads them:
+// shard pointers, one tensor map per shard, absolute destination
+// addresses (a block on the device, its pinned staging on the host). A plan
+// keeps kPtrSets of them, so that a caller alternating between a few
+// buffer sets (FSDP double buffering) reuses uploaded tables and never
+// waits for an upload.
+constexpr int kPtrSets = 4;
+struct PtrSet {
+  unsigned char* d_block = nullptr;
+  void* h_pinned = nullptr;
+  cudaEvent_t upload_done = nullptr;  // the last upload from h_pinned
+  bool uploaded = false;              // upload_done has been recorded
+  std::vector<const void*> shards;
+  std::vector<void*> pools;
+  bool shards_valid = false, pools_valid = false;
+  bool tmaps_dirty = false;           // maps rewritten since a launch used them
+  bool captured = false;              // a captured graph reads it: never replaced
+  uint64_t last_use = 0;
+};
+
 // Everything the host side of a plan owns.
 struct Plan {
   int device = -1;
@@ -162,21 +187,14 @@ struct Plan {
   std::vector<uint8_t> slot_used, slot_tmap;
   int32_t local_shard = -1;                 // >= 0: shard-local plan
 
-  // device side: one allocation for the static tables, one for the
-  // pointer tables that follow the caller's buffers
+  // device side: one allocation for the static tables and kPtrSets
+  // pointer-table blocks that follow the caller's buffers
   void* d_tables = nullptr;
   PrepArgs args{};                   // static parts filled at upload
-  const uint16_t** d_shard_ptrs = nullptr;      // dynamic block: shard ptrs,
-  unsigned char* d_tmaps = nullptr;             //   their tensor maps,
-  DevDstPtr* d_dst_ptrs = nullptr;              //   destination pointers
-  size_t dyn_bytes = 0;                         // size of that block
+  size_t dyn_bytes = 0;              // size of one pointer-table block
+  PtrSet sets[kPtrSets];
+  uint64_t use_clock = 0;            // for least-recently-used replacement
   int32_t* d_error = nullptr;
-  void* h_pinned = nullptr;          // pinned staging of the dynamic block
-  std::vector<const void*> cached_shards;
-  std::vector<void*> cached_pools;
-  bool shards_valid = false, pools_valid = false;
-  bool tmaps_dirty = false;          // rewritten since the last launch
-  cudaEvent_t ptr_upload_done = nullptr;
   cudaEvent_t last_done = nullptr;
   bool ran = false;
   int sm_count = 0;

@@ -57,6 +57,13 @@ constexpr int kStages = 4;                          // ring depth
 static_assert(kStages % kGroups == 0, "every stage must belong to one consumer group");
 constexpr int kStageBytes = kTile * kTile * 2;      // one BF16 block
 constexpr int kRowBytes = kTile * 2;                // one block row in a stage
+// A row that is not 16-byte aligned is copied as the 16-byte-aligned span
+// around it (at most 16 + 256 bytes) into a slot of its own, and the
+// consumers move it into place; a stage holds 128 such slots.
+constexpr int kSlotBytes = kRowBytes + 16;
+constexpr int kStageStride = kTile * kSlotBytes;
+// units per descriptor batch (one 32-byte descriptor per 8 lanes)
+constexpr int kBatch = 4;
 constexpr int kConsumerThreads = kGroups * kGroupThreads;
 constexpr int kCtaThreads = kConsumerThreads + 32;
 constexpr int kRowStride = kGroupThreads / 16;      // rows between a thread's rows
@@ -70,8 +77,9 @@ struct SmemCtl {
   float wmax[kGroups][2][kGroupWarps];   // per-warp block amax, double-buffered
   int abort_flag;
   uint32_t stored[kGroups];              // units whose stores each group has issued
+  uint8_t skew[kStages][kTile];          // unaligned rows: offset of the row in its slot
 };
-constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kStageBytes + sizeof(SmemCtl);
+constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kStageStride + sizeof(SmemCtl);
 static_assert(kSmemBytes <= 227 * 1024, "shared memory");
 
 // ---------------------------------------------------------------- PTX ---
@@ -195,53 +203,150 @@ __device__ __forceinline__ void give_up(const PrepArgs& a, SmemCtl& sm) {
 }
 
 // --------------------------------------------------------------- producer ---
-__device__ __forceinline__ uint32_t load_unit_word(const PrepArgs& a, int64_t first, int64_t n_local,
-                                                   int64_t batch, int lane) {
-  const int64_t k = 4 * batch + (lane >> 3);
-  if (k >= n_local) return 0;
-  const int64_t u = first + k * (int64_t)gridDim.x;
-  return ld_nc_u32(reinterpret_cast<const uint32_t*>(a.units + u) + (lane & 7));
+// Units come in batches of kBatch consecutive units of the schedule. With a
+// ticket counter (PrepArgs::ticket) every CTA takes the next free batch when
+// it needs one, so SMs that run faster take more batches and the launch ends
+// evenly; without one, CTA b takes units b, b + grid, b + 2 grid, ...
+struct Batch {
+  uint32_t word;   // lane l: word l % 8 of the batch's unit l / 8
+  int64_t first;   // the batch's first unit (static: its CTA-local index)
+  int n;           // units in the batch, 0 once the CTA's units are done
+};
+
+// Lane 0 takes the next ticket. The value is broadcast only when its batch
+// is loaded, a batch later, so the atomic's latency does not stall the warp.
+__device__ __forceinline__ uint32_t take_ticket(const PrepArgs& a, int lane) {
+  return lane == 0 ? atomicAdd(a.ticket, 1u) : 0u;
 }
 
-__device__ void producer(const PrepArgs& a, SmemCtl& sm, uint32_t stage0, int64_t first, int64_t n_local,
-                         int lane) {
+// Global unit index of unit j of a batch.
+__device__ __forceinline__ int64_t batch_unit(bool dyn, const Batch& bt, int j, int64_t first) {
+  return dyn ? bt.first + j : first + (bt.first + j) * (int64_t)gridDim.x;
+}
+
+__device__ __forceinline__ Batch load_batch(const PrepArgs& a, bool dyn, int64_t first, int64_t n_local,
+                                            int64_t index, int lane) {
+  Batch bt;
+  if (dyn) {
+    index = __shfl_sync(kFull, (uint32_t)index, 0);      // lane 0's ticket
+    bt.first = a.unit_begin + (int64_t)kBatch * index;
+    bt.n = (int)(a.unit_end <= bt.first ? 0 : a.unit_end - bt.first >= kBatch ? kBatch : a.unit_end - bt.first);
+  } else {
+    bt.first = (int64_t)kBatch * index;                   // CTA-local units
+    bt.n = (int)(n_local <= bt.first ? 0 : n_local - bt.first >= kBatch ? kBatch : n_local - bt.first);
+  }
+  bt.word = 0;
+  if ((lane >> 3) < bt.n)
+    bt.word = ld_nc_u32(reinterpret_cast<const uint32_t*>(a.units + batch_unit(dyn, bt, lane >> 3, first)) +
+                        (lane & 7));
+  return bt;
+}
+
+// Rows from several shards, or rows that are not 16-byte aligned: one bulk
+// copy per row (the full_tensor() row gather). A 16-byte-aligned row lands
+// at its place in the stage; any other row is copied as the 16-byte-aligned
+// span that holds it into its 272-byte slot, at offset skew = address % 16
+// (the span starts at most 15 bytes before the row and ends at most 15
+// after it; both ends lie in the 16-byte granules of the row's own first
+// and last bytes, so no page that the row does not touch is read), and the
+// consumers move it into place.
+__device__ __forceinline__ void load_rows(const PrepArgs& a, SmemCtl& sm, const uint32_t (&w)[8], int st,
+                                          uint32_t dst, uint32_t full, uint64_t pol, int lane) {
+  const int nrows = (int)(w[5] & 0xFFu) + 1;
+  const uint32_t row_bytes = (((w[5] >> 8) & 0xFFu) + 1u) * 2u;
+  const bool narrow = !((w[5] >> 16) & kUnitVec);
+  const int64_t N = w[4];
+  int run = (int)w[0];
+  uintptr_t src[kTile / 32];
+  uint32_t len[kTile / 32];
+  uint32_t total = 0;
+#pragma unroll
+  for (int i = 0; i < kTile / 32; ++i) {
+    const int r = lane + 32 * i;
+    src[i] = 0;
+    len[i] = 0;
+    if (r < nrows) {
+      const int64_t fr = (int64_t)w[1] + r;
+      while (fr >= a.runs[run].row0 + a.runs[run].rows) ++run;
+      const DevRun rn = a.runs[run];
+      const uintptr_t p = reinterpret_cast<uintptr_t>(a.shard_ptrs[rn.slot] + (fr - rn.row0) * N +
+                                                      (int64_t)w[3] * kTile);
+      if (narrow) {
+        src[i] = p & ~(uintptr_t)15;
+        len[i] = (uint32_t)(((p + row_bytes + 15) & ~(uintptr_t)15) - src[i]);
+        sm.skew[st][r] = (uint8_t)(p & 15);
+      } else {
+        src[i] = p;
+        len[i] = row_bytes;
+      }
+      total += len[i];
+    }
+  }
+  total = __reduce_add_sync(kFull, total);
+  __syncwarp();                 // the skews are written before the stage's arrival
+  if (lane == 0) mbar_arrive_tx(full, total);
+  __syncwarp();
+  const uint32_t stride = narrow ? (uint32_t)kSlotBytes : (uint32_t)kRowBytes;
+#pragma unroll
+  for (int i = 0; i < kTile / 32; ++i)
+    if (len[i]) bulk_load(dst + (uint32_t)(lane + 32 * i) * stride, reinterpret_cast<const void*>(src[i]),
+                          len[i], full, pol);
+}
+
+// dyn: units come from the ticket counter, else the static sequence.
+__device__ void producer(const PrepArgs& a, bool dyn, SmemCtl& sm, uint32_t stage0, int64_t first,
+                         int64_t n_local, int lane) {
   const uint64_t pol = load_policy();
-  // descriptors of four consecutive units per batch: lane l holds word
-  // l % 8 of unit l / 8; two batches are always in flight ahead
-  uint32_t cur = load_unit_word(a, first, n_local, 0, lane);
-  uint32_t nxt = load_unit_word(a, first, n_local, 1, lane);
+  // descriptors of a batch are loaded two batches ahead; with tickets, the
+  // ticket of a batch is taken one batch before its descriptors
+  int64_t idx[3] = {0, 1, 2};
+  if (dyn) {
+    idx[0] = take_ticket(a, lane);
+    idx[1] = take_ticket(a, lane);
+    idx[2] = take_ticket(a, lane);
+  }
+  Batch cur = load_batch(a, dyn, first, n_local, idx[0], lane);
+  Batch nxt = load_batch(a, dyn, first, n_local, idx[1], lane);
+  int64_t next_idx = idx[2];
   int64_t last_slot = -1;
-  int64_t k = 0;
+  int64_t k = 0;                // CTA-local sequence of stage uses
   bool ok = true;
-  for (int64_t b = 0; ok && k < n_local; ++b) {
-    const uint32_t nn = load_unit_word(a, first, n_local, b + 2, lane);
-    for (int j = 0; j < 4 && k < n_local; ++j, ++k) {
+  // wait until stage k % kStages is free; false (and give up) if the wait ran out
+  auto claim = [&](int st) {
+    bool got = true;
+    if (lane == 0) got = wait_bounded(smem_u32(&sm.empty[st]), (uint32_t)((k / kStages) & 1) ^ 1u,
+                                      a.timeout_ns, &sm.abort_flag);
+    if (!__shfl_sync(kFull, (int)got, 0)) {
+      if (lane == 0) give_up(a, sm);
+      return false;
+    }
+    return true;
+  };
+  while (ok && cur.n > 0) {
+    const Batch nn = load_batch(a, dyn, first, n_local, next_idx, lane);
+    if (dyn && nn.n > 0) next_idx = take_ticket(a, lane);
+    else next_idx += dyn ? 0 : 1;
+    for (int j = 0; j < cur.n; ++j, ++k) {
       uint32_t w[8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) w[i] = __shfl_sync(kFull, cur, 8 * j + i);
+      for (int i = 0; i < 8; ++i) w[i] = __shfl_sync(kFull, cur.word, 8 * j + i);
       const int st = (int)(k % kStages);
       const uint32_t full = smem_u32(&sm.full[st]);
-      bool got = true;
-      if (lane == 0) got = wait_bounded(smem_u32(&sm.empty[st]), (uint32_t)((k / kStages) & 1) ^ 1u,
-                                        a.timeout_ns, &sm.abort_flag);
-      if (!__shfl_sync(kFull, (int)got, 0)) {
-        if (lane == 0) give_up(a, sm);
+      if (!claim(st)) {
         ok = false;
         break;
       }
       // testing hook: leave this unit's stage unfilled, so that its
       // consumers' wait runs out
-      if (first + k * (int64_t)gridDim.x == a.stall_unit) continue;
+      if (batch_unit(dyn, cur, j, first) == a.stall_unit) continue;
       const uint32_t flags = w[5] >> 16;
-      const uint32_t dst = stage0 + (uint32_t)st * kStageBytes;
+      const uint32_t dst = stage0 + (uint32_t)st * kStageStride;
       if (lane == 0) {
         uint4* m = reinterpret_cast<uint4*>(&sm.meta[st]);
         m[0] = make_uint4(w[0], w[1], w[2], w[3]);
         m[1] = make_uint4(w[4], w[5], w[6], w[7]);
       }
-      if (!(flags & kUnitVec)) {
-        if (lane == 0) mbar_arrive(full);          // the consumers gather this one
-      } else if (!(flags & kUnitMulti)) {
+      if ((flags & kUnitVec) && !(flags & kUnitMulti)) {
         if (lane == 0) {
           const unsigned char* map = a.tmaps + (size_t)w[0] * kTmapBytes;
           if (a.tmap_fence && (int64_t)w[0] != last_slot) tmap_acquire(map);
@@ -250,24 +355,26 @@ __device__ void producer(const PrepArgs& a, SmemCtl& sm, uint32_t stage0, int64_
           tma_load_2d(dst, map, (int)(w[3] * kTile), (int)w[1], full, pol);
         }
       } else {
-        // rows from several shards: one bulk copy per row
-        const int nrows = (int)(w[5] & 0xFFu) + 1;
-        const uint32_t row_bytes = (((w[5] >> 8) & 0xFFu) + 1u) * 2u;
-        if (lane == 0) mbar_arrive_tx(full, row_bytes * (uint32_t)nrows);
-        __syncwarp();
-        const int64_t N = w[4];
-        int run = (int)w[0];
-        for (int r = lane; r < nrows; r += 32) {
-          const int64_t fr = (int64_t)w[1] + r;
-          while (fr >= a.runs[run].row0 + a.runs[run].rows) ++run;
-          const DevRun rn = a.runs[run];
-          const uint16_t* src = a.shard_ptrs[rn.slot] + (fr - rn.row0) * N + (int64_t)w[3] * kTile;
-          bulk_load(dst + (uint32_t)r * kRowBytes, src, row_bytes, full, pol);
-        }
+        load_rows(a, sm, w, st, dst, full, pol, lane);
       }
     }
     cur = nxt;
     nxt = nn;
+  }
+  // a ticket taken but not used (after an abort) must still have landed
+  // before this CTA counts itself done: wait for the atomic's return value
+  if (dyn) asm volatile("" ::"r"((uint32_t)next_idx) : "memory");
+  // one end marker per consumer group: an arrival with no copy
+  for (int e = 0; ok && e < kGroups; ++e, ++k) {
+    const int st = (int)(k % kStages);
+    if (!claim(st)) {
+      ok = false;
+      break;
+    }
+    if (lane == 0) {
+      sm.meta[st].shape = kUnitEnd << 16;
+      mbar_arrive(smem_u32(&sm.full[st]));
+    }
   }
   // no copy may still be landing in this CTA's shared memory when it exits:
   // wait for the last fill of every stage (completed fills return at once)
@@ -332,61 +439,45 @@ __device__ __forceinline__ Place place(const PrepArgs& a, const DevUnit& m, uint
   return pl;
 }
 
-// Rows that are not 16-byte aligned: the group gathers the block element by
-// element into the stage (zeros outside the block), warp w taking rows
-// w, w + 4, ..., lanes taking consecutive columns. Eight rows are loaded
-// before any is stored, so 32 loads per lane are in flight; a block whose
-// rows come from one shard needs no per-row run lookup.
-__device__ __forceinline__ const uint16_t* gather_row(const PrepArgs& a, const DevUnit& m, int& run,
-                                                      const uint16_t* one_shard, int r) {
-  const int64_t N = m.cols;
-  if (one_shard) return one_shard + (int64_t)r * N;
-  const int64_t fr = (int64_t)m.src_row + r;
-  while (fr >= a.runs[run].row0 + a.runs[run].rows) ++run;
-  const DevRun rn = a.runs[run];
-  return a.shard_ptrs[rn.slot] + (fr - rn.row0) * N + (int64_t)m.bj * kTile;
+// The thread's 16-byte chunk cc of an unaligned row held in its slot at
+// offset skew (even: rows are 2-byte aligned): four 4-byte loads, or five
+// and a 16-bit funnel shift when the chunk starts 2 bytes past a word.
+__device__ __forceinline__ uint4 ld_skewed(const uint8_t* slot, int skew, int cc) {
+  const uint32_t* w = reinterpret_cast<const uint32_t*>(slot + ((skew + 16 * cc) & ~3));
+  if ((skew & 2) == 0) return make_uint4(w[0], w[1], w[2], w[3]);
+  const uint32_t w4 = w[4];
+  return make_uint4(__funnelshift_r(w[0], w[1], 16), __funnelshift_r(w[1], w[2], 16),
+                    __funnelshift_r(w[2], w[3], 16), __funnelshift_r(w[3], w4, 16));
 }
 
-__device__ void gather_stage(const PrepArgs& a, const DevUnit& m, uint8_t* sp, int wg, int lane) {
-  constexpr int kRowsAtOnce = 8;
-  const int nrows = (int)(m.shape & 0xFFu) + 1, ncols = (int)((m.shape >> 8) & 0xFFu) + 1;
-  int run = (int)m.src;
-  const uint16_t* one_shard = nullptr;
-  if (!((m.shape >> 16) & kUnitMulti)) {
-    const DevRun rn = a.runs[run];
-    one_shard = a.shard_ptrs[rn.slot] + ((int64_t)m.src_row - rn.row0) * (int64_t)m.cols +
-                (int64_t)m.bj * kTile;
+// Zero the BF16 values of a chunk at and after index `valid` (0..8).
+__device__ __forceinline__ uint4 keep_first(uint4 v, int valid) {
+  if (valid >= 8) return v;
+  uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int k = 0; k < 4; ++k)
+    w[k] &= (2 * k < valid ? 0x0000FFFFu : 0u) | (2 * k + 1 < valid ? 0xFFFF0000u : 0u);
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// Rows that are not 16-byte aligned arrive in slots (see load_rows): read
+// the thread's chunks from them, zero what lies outside the block, and,
+// once the whole group has read, write them back at their places in the
+// stage, where the general store routines read them again.
+__device__ __forceinline__ void realign_stage(const SmemCtl& sm, int st, uint8_t* sp, int nrows, int ncols,
+                                              int r0, int cc, int bar_id, uint4 (&v)[kRows]) {
+  const int valid = ncols - 8 * cc;
+#pragma unroll
+  for (int j = 0; j < kRows; ++j) {
+    const int r = r0 + kRowStride * j;
+    v[j] = make_uint4(0, 0, 0, 0);
+    if (r < nrows && valid > 0) v[j] = keep_first(ld_skewed(sp + r * kSlotBytes, sm.skew[st][r], cc), valid);
   }
-  for (int rb = wg; rb < kTile; rb += kGroupWarps * kRowsAtOnce) {
-    // lane l takes the element pairs l and l + 32 of each row: one 4-byte
-    // load where the row start is 4-byte aligned (an even row length in a
-    // 4-byte aligned shard), else two 2-byte loads; nothing past column
-    // ncols - 1 is read
-    uint32_t e[kRowsAtOnce][kTile / 64];
+  bar_sync(bar_id, kGroupThreads);
 #pragma unroll
-    for (int i = 0; i < kRowsAtOnce; ++i) {
-      const int r = rb + i * kGroupWarps;
-      const uint16_t* row = r < nrows ? gather_row(a, m, run, one_shard, r) : nullptr;
-      const bool w4 = row && (reinterpret_cast<uintptr_t>(row) & 3u) == 0;
-#pragma unroll
-      for (int c2 = 0; c2 < kTile / 64; ++c2) {
-        const int c = 2 * (lane + 32 * c2);
-        if (w4 && c + 1 < ncols) {
-          e[i][c2] = ld_nc_u32(row + c);
-        } else {
-          const uint32_t lo = (row && c < ncols) ? ld_nc_u16(row + c) : 0u;
-          const uint32_t hi = (row && c + 1 < ncols) ? ld_nc_u16(row + c + 1) : 0u;
-          e[i][c2] = lo | (hi << 16);
-        }
-      }
-    }
-#pragma unroll
-    for (int i = 0; i < kRowsAtOnce; ++i) {
-      uint32_t* out = reinterpret_cast<uint32_t*>(sp + (rb + i * kGroupWarps) * kRowBytes);
-#pragma unroll
-      for (int c2 = 0; c2 < kTile / 64; ++c2) out[lane + 32 * c2] = e[i][c2];
-    }
-  }
+  for (int j = 0; j < kRows; ++j)
+    *reinterpret_cast<uint4*>(sp + (r0 + kRowStride * j) * kRowBytes + cc * 16) = v[j];
+  fence_proxy_async_smem();          // the stage is refilled by copies later
 }
 
 // Codes of one row chunk where rows are not 8-byte aligned; `valid` bytes
@@ -511,13 +602,13 @@ __device__ __noinline__ void store_bf16_general(const PrepArgs& a, const DevUnit
 }
 
 template <bool kDebug, bool kSignal>
-__device__ void consumer(const PrepArgs& a, SmemCtl& sm, uint8_t* stages, int64_t n_local, int g, int t) {
+__device__ void consumer(const PrepArgs& a, SmemCtl& sm, uint8_t* stages, int g, int t) {
   const int lane = t & 31, wg = t >> 5;
   const int cc = t & 15;       // 16-byte column chunk
   const int r0 = t >> 4;       // first row; rows r0 + kRowStride j
   const int bar_id = 1 + g;
   int it = 0;
-  for (int64_t k = g; k < n_local; k += kGroups, ++it) {
+  for (int64_t k = g;; k += kGroups, ++it) {
     const int st = (int)(k % kStages);
     const bool ok = wait_bounded(smem_u32(&sm.full[st]), (uint32_t)((k / kStages) & 1), a.timeout_ns,
                                  &sm.abort_flag);
@@ -529,21 +620,19 @@ __device__ void consumer(const PrepArgs& a, SmemCtl& sm, uint8_t* stages, int64_
       const uint4 m1 = reinterpret_cast<const uint4*>(&sm.meta[st])[1];
       m = DevUnit{m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
     }
+    const uint32_t flags = m.shape >> 16;
+    if (flags & kUnitEnd) return;       // the producer has no more units
     const DevDstPtr dp0 = load_dst<kDebug>(a, m.dst_begin);
     const Place pl0 = place(a, m, m.dst_begin, r0, cc);
-    const uint32_t flags = m.shape >> 16;
     const int nrows = (int)(m.shape & 0xFFu) + 1, ncols = (int)((m.shape >> 8) & 0xFFu) + 1;
     const bool whole = (m.shape & 0xFFFFu) == 0x7F7Fu;
     const bool vec = flags & kUnitVec;
-    uint8_t* sp = stages + (size_t)st * kStageBytes;
-    if (!vec) {
-      gather_stage(a, m, sp, wg, lane);
-      fence_proxy_async_smem();          // the stage is refilled by copies later
-      bar_sync(bar_id, kGroupThreads);
-    }
+    uint8_t* sp = stages + (size_t)st * kStageStride;
     uint4 v[kRows];
     const uint8_t* tp = sp + r0 * kRowBytes + cc * 16;
-    if (whole) {
+    if (!vec) {
+      realign_stage(sm, st, sp, nrows, ncols, r0, cc, bar_id, v);
+    } else if (whole) {
 #pragma unroll
       for (int j = 0; j < kRows; ++j) v[j] = *reinterpret_cast<const uint4*>(tp + j * kRowStride * kRowBytes);
     } else {
@@ -692,8 +781,10 @@ __global__ void __launch_bounds__(kSignal ? kCtaThreads + 32 : kCtaThreads, 1)
     prep_kernel(const __grid_constant__ PrepArgs a) {
   extern __shared__ unsigned char smem_raw[];
   uint8_t* stages = reinterpret_cast<uint8_t*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-  SmemCtl& sm = *reinterpret_cast<SmemCtl*>(stages + (size_t)kStages * kStageBytes);
+  SmemCtl& sm = *reinterpret_cast<SmemCtl*>(stages + (size_t)kStages * kStageStride);
   const int tid = threadIdx.x;
+  // static assignment (per-block counting, or no ticket): CTA b takes units
+  // first, first + grid, ...; the signal warp walks the same sequence
   const int64_t first = a.unit_begin + blockIdx.x;
   const int64_t n_local = first < a.unit_end ? (a.unit_end - first + gridDim.x - 1) / gridDim.x : 0;
   if (tid == 0) {
@@ -706,13 +797,24 @@ __global__ void __launch_bounds__(kSignal ? kCtaThreads + 32 : kCtaThreads, 1)
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
-  if (n_local == 0) return;
   if (tid >= kCtaThreads) {
     if (tid == kCtaThreads) signal_warp(a, sm, first, n_local);   // kSignal only
   } else if (tid >= kConsumerThreads) {
-    producer(a, sm, smem_u32(stages), first, n_local, tid & 31);
+    producer(a, !kSignal && a.ticket, sm, smem_u32(stages), first, n_local, tid & 31);
   } else {
-    consumer<kDebug, kSignal>(a, sm, stages, n_local, tid / kGroupThreads, tid % kGroupThreads);
+    consumer<kDebug, kSignal>(a, sm, stages, tid / kGroupThreads, tid % kGroupThreads);
+  }
+  if (kSignal || !a.ticket) return;
+  // the last CTA to finish resets the ticket counter for the next launch:
+  // every CTA takes its last ticket before it counts itself done
+  __syncthreads();
+  if (tid == 0) {
+    __threadfence();
+    if (atomicAdd(a.ticket + 1, 1u) == gridDim.x - 1) {
+      *reinterpret_cast<volatile uint32_t*>(a.ticket) = 0u;
+      *reinterpret_cast<volatile uint32_t*>(a.ticket + 1) = 0u;
+      __threadfence();
+    }
   }
 }
 

@@ -77,11 +77,21 @@ def halo_transfers(w, fsdp: int) -> List[tuple]:
     return out
 
 
-def exchange_halos(w, transfers, rank: int, own_shards, group=None) -> dict:
+def halo_buffers(w, transfers, rank: int, device) -> dict:
+    """Receive buffers for this rank's halos, {(param, shard): [rows, cols]
+    BF16 tensor}: allocated once, so that every step's exchange lands at the
+    same addresses (a plan then reuses its pointer tables)."""
+    import torch
+    return {(p, k): torch.empty((n, w.params[p].cols), dtype=torch.bfloat16, device=device)
+            for src, dst, p, k, n in transfers if dst == rank and src != rank}
+
+
+def exchange_halos(w, transfers, rank: int, own_shards, group=None, out=None) -> dict:
     """Send the leading rows of this rank's shards that other ranks need and
     receive this rank's halos. own_shards[p] is this rank's shard of param p
     (a [shard_rows, cols] BF16 tensor on the group's device). Returns
-    {(param, shard): [rows, cols] tensor} of the received halo rows."""
+    {(param, shard): [rows, cols] tensor} of the received halo rows, written
+    into `out` (from halo_buffers) when given, else into new tensors."""
     import torch
     import torch.distributed as dist
     ops, got = [], {}
@@ -97,8 +107,12 @@ def exchange_halos(w, transfers, rank: int, own_shards, group=None) -> dict:
             t = own_shards[p][:n].contiguous().view(torch.int16)
             ops.append(dist.P2POp(dist.isend, t, dst, group=group, tag=tag))
         elif dst == rank and src != rank:
-            buf = torch.empty((n, w.params[p].cols), dtype=torch.int16, device=dev)
-            got[(p, k)] = buf.view(torch.bfloat16)
+            if out is not None:
+                got[(p, k)] = out[(p, k)]
+                buf = out[(p, k)].view(torch.int16)
+            else:
+                buf = torch.empty((n, w.params[p].cols), dtype=torch.int16, device=dev)
+                got[(p, k)] = buf.view(torch.bfloat16)
             ops.append(dist.P2POp(dist.irecv, buf, src, group=group, tag=tag))
     if ops:
         for q in dist.batch_isend_irecv(ops):

@@ -249,13 +249,20 @@ wt_status wt_plan_get_stats(const wt_plan* p, wt_plan_stats* stats);
  *   wt_plan_pool_bytes bytes (NULL allowed for a 0-byte pool).
  * Shards and pools are borrowed: they must stay valid until the stream
  * work completes. Asynchronous: no allocation, no device synchronisation.
- * The pointer tables are re-uploaded (one stream-ordered copy) only when
- * they differ from the previous call's. Calls on one plan must be ordered
- * on one stream (the plan holds one device pointer table).
+ * The plan keeps the device tables of the last four distinct (shard_ptrs,
+ * pools) sets it was given; a call with a known set uploads nothing, a new
+ * set replaces the least recently used one with one stream-ordered copy
+ * (and tensor maps encoded on the host for the shards that changed). A
+ * caller alternating between up to four buffer sets therefore never waits;
+ * the only host wait is for the upload of the replaced set, four new sets
+ * back. Calls on one plan must be ordered on one stream.
  * CUDA graphs: a call may be captured once an uncaptured call has staged
  * the same shard and pool pointers (a captured call with new pointers
- * returns WT_ERR_INVALID_ARGUMENT). The plan does not track the graph's
- * replays: finish them before destroying the plan or changing pointers.
+ * returns WT_ERR_INVALID_ARGUMENT). A set that a capture used is kept for
+ * the plan's lifetime, so its graph stays valid however many other sets
+ * are used later; once all four sets are held by captures, new pointers
+ * return WT_ERR_INVALID_ARGUMENT. Finish a graph's replays before
+ * destroying the plan.
  * Errors: WT_ERR_INVALID_ARGUMENT (null pointer where data is needed,
  * host-only plan), WT_ERR_ALIGNMENT, WT_ERR_CUDA (a launch or copy failed,
  * including an earlier asynchronous error). */
