@@ -5,8 +5,10 @@ ranks; 16.96 G params, 33.9 GB BF16 read, 16.96 GB written per step).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
                   [--workload kimi_k2_moe_layer|llama_dense|llama_dense_tp4|edge_stress|
-                              tiny_dense|offload_8layer] [--images K]
-                  [--no-e2e] [--no-cpu-baseline] [--experts E]
+                              edge_narrow|edge_narrow_1|tiny_dense|offload_8layer|tokens]
+                  [--partition replicas|sources] [--sources S] [--shard-local [--fsdp F] [--halo]]
+                  [--counters launch|rank] [--images K] [--no-e2e] [--no-cpu-baseline]
+                  [--experts E]
 
 Prints one JSON line. `value` is GB/s of BF16 input for the whole job
 (all ranks), timed with CUDA events on the launching stream around K
@@ -51,8 +53,8 @@ L2_BYTES = 126 * 10**6
 # from the ncu capture summarised in profiles/ (16 experts, scaled by the
 # blocks processed to the 385-expert layer); valid only for the kernel
 # source it was taken on.
-TRAFFIC = {"kernel_sha256": "dac764ecee6e1a928a0a218d1f4121e034f88a6e7188e07dc5a483d45cb8aa75",
-           "bytes_per_launch": 50000621440, "experts": 385}
+TRAFFIC = {"kernel_sha256": "9acb5d282c5b9c94e37d63ef7558f71736e5faa07d04b86b21edd34ad3f16794",
+           "bytes_per_launch": 50023547035, "experts": 385}
 
 
 def kernel_sha() -> str:
@@ -244,6 +246,30 @@ def rank_work(workload, partition: str, world: int, rank: int, fsdp: int = 0,
     raise ValueError(partition)
 
 
+def rank_groups(w) -> int:
+    """Non-empty rank groups of a workload (blocks grouped by the lowest
+    rank that holds them): the launches of one step counted per rank."""
+    groups = set()
+    for o, out in enumerate(w.outputs):
+        if out.slices is None or all(sl is None for sl in out.slices):
+            groups.add(min(out.dst_ranks))
+            continue
+        m, n = w.output_shape(o)
+
+        def holds(sl, bi, bj):
+            if sl is None:
+                return True
+            dim, ranges = sl
+            b = bi if dim == 0 else bj
+            return any(r0 // 128 <= b < -(-(r0 + ln) // 128) for r0, ln in ranges)
+
+        for bi in range(-(-m // 128)):
+            for bj in range(-(-n // 128)):
+                held = [r for r, sl in zip(out.dst_ranks, out.slices) if holds(sl, bi, bj)]
+                groups.add(min(held) if held else 0)
+    return len(groups)
+
+
 def sample_outputs(w, experts: int, target_bytes: int = 700_000_000) -> list:
     """A bounded sample of a workload's outputs: the first `experts` experts
     of an MoE layer, else the outputs in plan order up to about
@@ -368,7 +394,7 @@ def main():
                     help="experts per reference step (raised to one output per host core)")
     ap.add_argument("--workload", default="kimi_k2_moe_layer",
                     choices=["kimi_k2_moe_layer", "llama_dense", "llama_dense_tp4", "edge_stress",
-                             "tiny_dense", "offload_8layer", "tokens"])
+                             "edge_narrow", "edge_narrow_1", "tiny_dense", "offload_8layer", "tokens"])
     ap.add_argument("--shard-local", action="store_true",
                     help="FSDP group of --fsdp ranks sharing one layer; each prepares its own shard")
     ap.add_argument("--fsdp", type=int, default=0, help="FSDP degree for --shard-local (0: world)")
@@ -380,7 +406,7 @@ def main():
     ap.add_argument("--sources", type=int, default=0,
                     help="with --partition sources: number of source GPUs (0: world size); "
                          "at one GPU, --sources 8 times rank 0's share")
-    ap.add_argument("--counters", choices=["launch", "block"], default=None,
+    ap.add_argument("--counters", choices=["launch", "rank"], default=None,
                     help="time the step with per-rank completion counters")
     ap.add_argument("--tokens", type=int, default=131072)
     ap.add_argument("--hidden", type=int, default=7168)
@@ -463,7 +489,7 @@ def main():
     if args.counters:
         counters = torch.zeros(w.num_ranks, dtype=torch.int32, device=dev)
         plan.set_counters(counters.data_ptr(),
-                          wt.WT_COUNT_PER_BLOCK if args.counters == "block" else wt.WT_COUNT_PER_LAUNCH)
+                          wt.WT_COUNT_PER_RANK if args.counters == "rank" else wt.WT_COUNT_PER_LAUNCH)
     stream = torch.cuda.Stream(dev)
     sp = stream.cuda_stream
 
@@ -591,8 +617,10 @@ def main():
         "first_step_host_ms": round(first_step_host_ms, 2), "shards": st["num_slots"],
         "completion_counters": args.counters,
         "e2e": e2e, "cpu_baseline": cpu, "clocks": clk,
-        # the preparation kernel, plus the count kernel when counting per launch
-        "gpu_launches": args.steps * (2 if args.counters == "launch" else 1),
+        # the preparation kernel, plus the count kernel when counting per
+        # launch; per rank, one of each per non-empty rank group
+        "gpu_launches": args.steps * (2 if args.counters == "launch" else
+                                      2 * rank_groups(w) if args.counters == "rank" else 1),
         "wall_s_timed": round(t_wall, 4),
     }
     if rank == 0:

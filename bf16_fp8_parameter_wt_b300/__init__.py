@@ -2,7 +2,7 @@
 transfer: FSDP shard reassembly, projection fusion, BF16 -> FP8 e4m3
 128x128 block quantisation and packing into destination pools, as a C-ABI
 CUDA library (libwt.so, include/wt.h) with this thin binding."""
-from .wt import (EXPORTS, LIB_PATH, WT_COUNT_PER_BLOCK, WT_COUNT_PER_LAUNCH, WT_FLAG_DEBUG_CHECKS,
+from .wt import (EXPORTS, LIB_PATH, WT_COUNT_PER_RANK, WT_COUNT_PER_LAUNCH, WT_FLAG_DEBUG_CHECKS,
                  WT_FLAG_FORCE_NARROW, WT_FLAG_SHARD_HALO, WT_FLAG_SHARD_LOCAL, WT_OFFSET_AUTO, WT_OUT_BF16, WT_OUT_FP8_E4M3_B128, Plan,
                  PlanDesc, WTError, lib, wt_debug_fail_offload_chunk, wt_debug_stall_unit,
                  wt_last_error, wt_plan_check, wt_plan_create, wt_plan_destroy,
@@ -12,7 +12,7 @@ from .wt import (EXPORTS, LIB_PATH, WT_COUNT_PER_BLOCK, WT_COUNT_PER_LAUNCH, WT_
                  wt_wait_counters)
 
 __all__ = [
-    "WT_COUNT_PER_BLOCK", "WT_COUNT_PER_LAUNCH",
+    "WT_COUNT_PER_RANK", "WT_COUNT_PER_LAUNCH",
     "EXPORTS", "LIB_PATH", "WT_FLAG_DEBUG_CHECKS", "WT_FLAG_FORCE_NARROW", "WT_FLAG_SHARD_HALO", "WT_FLAG_SHARD_LOCAL", "WT_OFFSET_AUTO",
     "WT_OUT_BF16", "WT_OUT_FP8_E4M3_B128", "Plan", "PlanDesc", "WTError", "lib",
     "wt_debug_fail_offload_chunk", "wt_debug_stall_unit", "wt_last_error", "wt_plan_check", "wt_plan_create",

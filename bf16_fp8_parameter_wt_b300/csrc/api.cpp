@@ -115,7 +115,9 @@ wt_status upload(Plan& p, int device) {
   const size_t o_runs = take(p.h_runs.size() * sizeof(DevRun));
   const size_t o_geom = take(p.h_geom.size() * sizeof(DevDstGeom));
   const size_t o_bmap = take(p.h_blockmap.size() * sizeof(int32_t));
-  const size_t o_drank = take(p.h_dst_rank.size() * sizeof(int32_t));
+  const size_t o_perm = take(p.rank_perm.size() * sizeof(uint32_t));
+  const size_t o_gcounts = take(p.group_counts.size() * sizeof(uint32_t));
+  const size_t o_lperm = take(p.launch_perm.size() * sizeof(uint32_t));
   // per-rank block counts of a whole step and of each offload chunk
   std::vector<uint32_t> lc((1 + p.chunks.size()) * (size_t)p.num_ranks, 0);
   for (int32_t r = 0; r < p.num_ranks; ++r) lc[(size_t)r] = (uint32_t)p.expected_blocks[(size_t)r];
@@ -140,7 +142,9 @@ wt_status upload(Plan& p, int device) {
       (e = put(o_runs, p.h_runs.data(), p.h_runs.size() * sizeof(DevRun))) != cudaSuccess ||
       (e = put(o_geom, p.h_geom.data(), p.h_geom.size() * sizeof(DevDstGeom))) != cudaSuccess ||
       (e = put(o_bmap, p.h_blockmap.data(), p.h_blockmap.size() * sizeof(int32_t))) != cudaSuccess ||
-      (e = put(o_drank, p.h_dst_rank.data(), p.h_dst_rank.size() * sizeof(int32_t))) != cudaSuccess ||
+      (e = put(o_perm, p.rank_perm.data(), p.rank_perm.size() * sizeof(uint32_t))) != cudaSuccess ||
+      (e = put(o_gcounts, p.group_counts.data(), p.group_counts.size() * sizeof(uint32_t))) != cudaSuccess ||
+      (e = put(o_lperm, p.launch_perm.data(), p.launch_perm.size() * sizeof(uint32_t))) != cudaSuccess ||
       (e = put(o_lc, lc.data(), lc.size() * sizeof(uint32_t))) != cudaSuccess ||
       (e = cudaMemset(base + o_err, 0, sizeof(int32_t))) != cudaSuccess ||
       (e = cudaMemset(base + o_ticket, 0, 2 * sizeof(uint32_t))) != cudaSuccess)
@@ -151,7 +155,9 @@ wt_status upload(Plan& p, int device) {
   p.args.runs = reinterpret_cast<const DevRun*>(base + o_runs);
   p.args.ticket = reinterpret_cast<uint32_t*>(base + o_ticket);
   p.args.geom = reinterpret_cast<const DevDstGeom*>(base + o_geom);
-  p.args.dst_rank = reinterpret_cast<const int32_t*>(base + o_drank);
+  p.d_perm = reinterpret_cast<const uint32_t*>(base + o_perm);
+  p.d_group_counts = reinterpret_cast<const uint32_t*>(base + o_gcounts);
+  p.d_launch_perm = p.launch_perm.empty() ? nullptr : reinterpret_cast<const uint32_t*>(base + o_lperm);
   p.d_launch_counts = reinterpret_cast<uint32_t*>(base + o_lc);
   p.args.blockmap = reinterpret_cast<const int32_t*>(base + o_bmap);
   p.args.error_word = p.d_error;
@@ -427,14 +433,31 @@ wt_status wt_prepare(wt_plan* h, const void* const* shard_ptrs, void* const* poo
   a.stall_unit = p.stall_unit;
   a.timeout_ns = p.wait_limit_ns ? p.wait_limit_ns : kDefaultTimeoutNs;
   a.tmap_fence = ps.tmaps_dirty ? 1u : 0u;
-  a.counters = p.count_mode == WT_COUNT_PER_BLOCK ? p.counters : nullptr;
-  a.unit_begin = 0;
-  a.unit_end = p.num_units;
-  e = launch_prepare(a, grid_for(p, p.num_units), s, p.flags & WT_FLAG_DEBUG_CHECKS);
-  if (e != cudaSuccess) return cuda_fail(e, "preparation kernel launch");
-  if (p.counters && p.count_mode == WT_COUNT_PER_LAUNCH &&
-      (e = launch_add_counts(p.counters, p.d_launch_counts, p.num_ranks, p.d_error, s)) != cudaSuccess)
-    return cuda_fail(e, "completion count launch");
+  const bool debug = p.flags & WT_FLAG_DEBUG_CHECKS;
+  if (p.counters && p.count_mode == WT_COUNT_PER_RANK) {
+    // rank by rank: the units whose lowest holding rank is g, then their
+    // counts; after launch g, ranks 0..g have all their blocks
+    a.perm = p.d_perm;
+    for (int32_t g = 0; g < p.num_ranks; ++g) {
+      a.unit_begin = p.group_begin[(size_t)g];
+      a.unit_end = p.group_begin[(size_t)g + 1];
+      if (a.unit_end == a.unit_begin) continue;
+      if ((e = launch_prepare(a, grid_for(p, a.unit_end - a.unit_begin), s, debug)) != cudaSuccess)
+        return cuda_fail(e, "preparation kernel launch");
+      if ((e = launch_add_counts(p.counters, p.d_group_counts + (size_t)g * (size_t)p.num_ranks, p.num_ranks,
+                                 p.d_error, s)) != cudaSuccess)
+        return cuda_fail(e, "completion count launch");
+    }
+  } else {
+    a.perm = p.d_launch_perm;
+    a.unit_begin = 0;
+    a.unit_end = p.num_units;
+    e = launch_prepare(a, grid_for(p, p.num_units), s, debug);
+    if (e != cudaSuccess) return cuda_fail(e, "preparation kernel launch");
+    if (p.counters &&
+        (e = launch_add_counts(p.counters, p.d_launch_counts, p.num_ranks, p.d_error, s)) != cudaSuccess)
+      return cuda_fail(e, "completion count launch");
+  }
   if (capturing) return WT_OK;         // the graph's replays are the caller's to track
   ps.tmaps_dirty = false;
   if ((e = cudaEventRecord(p.last_done, s)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
@@ -466,9 +489,9 @@ wt_status wt_prepare_offload(wt_plan* h, const void* host_image, void* const* po
   bind_set(p, p.sets[set], a);
   a.shard_ptrs = p.d_offload_shard_ptrs;
   a.tmaps = p.d_offload_tmaps;
-  a.counters = p.count_mode == WT_COUNT_PER_BLOCK ? p.counters : nullptr;
   a.stall_unit = p.stall_unit;
   a.timeout_ns = p.wait_limit_ns ? p.wait_limit_ns : kDefaultTimeoutNs;
+  a.perm = p.d_launch_perm;          // keeps every chunk's unit range
   const char* host = static_cast<const char*>(host_image);
   auto drain = [&](wt_status s_, const std::string& msg) {
     cudaStreamSynchronize(cs);
@@ -498,7 +521,7 @@ wt_status wt_prepare_offload(wt_plan* h, const void* host_image, void* const* po
                             p.flags & WT_FLAG_DEBUG_CHECKS)) != cudaSuccess)
       return drain(WT_ERR_CUDA, std::string("preparation kernel launch: ") + cudaGetErrorString(e));
     if (c.unit_end > c.unit_begin) p.offload_tmaps_dirty = false;
-    if (p.counters && p.count_mode == WT_COUNT_PER_LAUNCH &&
+    if (p.counters &&
         (e = launch_add_counts(p.counters, p.d_launch_counts + (1 + i) * (size_t)p.num_ranks, p.num_ranks,
                                p.d_error, ks)) != cudaSuccess)
       return drain(WT_ERR_CUDA, std::string("completion count launch: ") + cudaGetErrorString(e));
@@ -539,7 +562,7 @@ wt_status wt_debug_fail_offload_chunk(wt_plan* h, int32_t chunk) {
 wt_status wt_plan_set_counters(wt_plan* h, uint32_t* counters, uint32_t mode) {
   if (!h) return fail(WT_ERR_INVALID_ARGUMENT, "plan is NULL");
   if (h->p.device < 0 && counters) return fail(WT_ERR_INVALID_ARGUMENT, "host-only plan cannot signal");
-  if (mode != WT_COUNT_PER_LAUNCH && mode != WT_COUNT_PER_BLOCK)
+  if (mode != WT_COUNT_PER_LAUNCH && mode != WT_COUNT_PER_RANK)
     return fail(WT_ERR_INVALID_ARGUMENT, "unknown counting mode");
   if (reinterpret_cast<uintptr_t>(counters) % 4) return fail(WT_ERR_ALIGNMENT, "counters must be 4-byte aligned");
   h->p.counters = counters;

@@ -174,8 +174,7 @@ extern "C" wt_status wt_prepare_noalloc(const wt_plan_desc* desc, const void* co
   a.tmap_fence = 1;                    // the maps were just rewritten
   a.timeout_ns = g_wait_limit_ns ? g_wait_limit_ns : kDefaultTimeoutNs;
   a.stall_unit = g_stall_unit;
-  a.counters = nullptr;
-  a.dst_rank = nullptr;
+  a.perm = nullptr;
   a.runs = reinterpret_cast<const DevRun*>(dbase + o_runs);
   a.shard_ptrs = reinterpret_cast<const uint16_t* const*>(dbase + o_shards);
   a.dst_ptrs = reinterpret_cast<const DevDstPtr*>(dbase + o_dsts);

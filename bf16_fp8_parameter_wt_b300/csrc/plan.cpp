@@ -258,6 +258,8 @@ wt_status compile_plan(const wt_plan_desc* d, Plan* p) {
   p->h_blockmap.clear();
   p->h_dst_rank.clear();
   p->expected_blocks.assign((size_t)p->num_ranks, 0);
+  p->group_counts.assign((size_t)p->num_ranks * (size_t)p->num_ranks, 0);
+  std::vector<int32_t> unit_group, held_ranks;
   p->h_units.reserve((size_t)units);
   p->slot_rows.assign(p->num_slots, 0);
   p->slot_cols.assign(p->num_slots, 0);
@@ -363,17 +365,26 @@ wt_status compile_plan(const wt_plan_desc* d, Plan* p) {
         u.dst_begin = (uint32_t)oi.dst_begin;
         // the destinations that hold this block; what the step moves is
         // counted from the units it runs
-        int32_t held = 0, which = -1;
+        int32_t held = 0, which = -1, min_rank = -1;
         const uint64_t elems = uint64_t(nrows * ncols);
+        held_ranks.clear();
         for (size_t d = 0; d < oi.dsts.size(); ++d) {
           const DevDstGeom& g = p->h_geom[(size_t)oi.dst_begin + d];
           const bool in = g.dim < 0 || p->h_blockmap[(size_t)g.map_off + (size_t)(g.dim == 0 ? bi : bj)] >= 0;
           if (!in) continue;
           ++held;
           which = (int32_t)d;
-          p->expected_blocks[(size_t)oi.dsts[d].rank] += 1;
+          const int32_t rk = oi.dsts[d].rank;
+          p->expected_blocks[(size_t)rk] += 1;
           p->bytes_written += elems * esize + (esize == 1 ? 4u : 0u);
+          held_ranks.push_back(rk);
+          if (min_rank < 0 || rk < min_rank) min_rank = rk;
         }
+        // rank groups: a unit belongs to the group of the lowest rank that
+        // holds its block (group 0 if none does)
+        const int32_t grp = std::max(min_rank, 0);
+        unit_group.push_back(grp);
+        for (int32_t rk : held_ranks) ++p->group_counts[(size_t)grp * (size_t)p->num_ranks + (size_t)rk];
         p->bytes_read += elems * 2u;
         p->num_params_total += (int64_t)elems;
         // when exactly one destination holds it, the unit names that one
@@ -389,6 +400,29 @@ wt_status compile_plan(const wt_plan_desc* d, Plan* p) {
   }
   p->num_dst_entries = dst_entries;
   p->num_units = (int64_t)p->h_units.size();
+  // Units whose rows are gathered one bulk copy per row (rows from several
+  // shards, or rows that are not 16-byte aligned) take several times as
+  // long as a tensor-copied block; a launch hands them out first, so that
+  // they overlap the streaming blocks instead of forming its tail.
+  auto slow = [&](int64_t u) {
+    const uint32_t f = p->h_units[(size_t)u].shape >> 16;
+    return (f & kUnitMulti) || !(f & kUnitVec);
+  };
+  // units in rank-group order, slow units first within a group, plan order
+  // otherwise, and where each group starts
+  p->rank_perm.resize((size_t)p->num_units);
+  p->group_begin.assign((size_t)p->num_ranks + 1, 0);
+  for (int32_t g : unit_group) ++p->group_begin[(size_t)g + 1];
+  for (int32_t r = 0; r < p->num_ranks; ++r) p->group_begin[(size_t)r + 1] += p->group_begin[(size_t)r];
+  {
+    std::vector<int64_t> at(p->group_begin.begin(), p->group_begin.end() - 1);
+    for (int pass = 0; pass < 2; ++pass)
+      for (int64_t u = 0; u < p->num_units; ++u)
+        if (slow(u) == (pass == 0)) p->rank_perm[(size_t)at[(size_t)unit_group[(size_t)u]]++] = (uint32_t)u;
+  }
+  // the order of a whole-step launch (and of each offload chunk, whose unit
+  // range it keeps): slow units first; left empty when there are none
+  p->launch_perm.clear();
   for (int32_t s = 0; s < p->num_slots; ++s) p->slot_used[(size_t)s] = p->slot_read_rows[(size_t)s] > 0;
 
   // ---- packed host image for offload and its chunks ----------------------
@@ -430,6 +464,18 @@ wt_status compile_plan(const wt_plan_desc* d, Plan* p) {
       p->chunks.push_back(c);
       o = e;
     }
+  }
+  bool any_slow = false;
+  for (int64_t u = 0; u < p->num_units && !any_slow; ++u) any_slow = slow(u);
+  if (any_slow) {
+    std::vector<std::pair<int64_t, int64_t>> ranges;
+    for (const Chunk& c : p->chunks) ranges.push_back({c.unit_begin, c.unit_end});
+    if (ranges.empty()) ranges.push_back({0, p->num_units});
+    p->launch_perm.reserve((size_t)p->num_units);
+    for (const auto& rg : ranges)
+      for (int pass = 0; pass < 2; ++pass)
+        for (int64_t u = rg.first; u < rg.second; ++u)
+          if (slow(u) == (pass == 0)) p->launch_perm.push_back((uint32_t)u);
   }
   return WT_OK;
 }

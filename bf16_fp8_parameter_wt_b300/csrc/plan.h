@@ -88,8 +88,6 @@ struct PrepArgs {
   const int32_t* blockmap;
   int64_t unit_begin, unit_end;
   int32_t* error_word;               // kErr* bits
-  uint32_t* counters;                // per-rank completion counters, or NULL
-  const int32_t* dst_rank;           // per destination entry: its rank
   uint64_t timeout_ns;               // limit of every wait inside the kernel
   uint32_t tmap_fence;               // tensor maps were rewritten since the last launch
   int64_t stall_unit;                // testing: this unit is never filled (-1: none)
@@ -97,6 +95,9 @@ struct PrepArgs {
   // next ticket (a batch of kBatch consecutive units) and the CTAs done.
   // NULL: units are assigned statically (CTA b takes b, b + grid, ...).
   uint32_t* ticket;
+  // NULL, or the launch runs units perm[unit_begin .. unit_end) (a rank
+  // group's units, see Plan::rank_perm)
+  const uint32_t* perm;
 };
 
 // Host-side copy of one param.
@@ -179,6 +180,17 @@ struct Plan {
   std::vector<int32_t> h_blockmap;
   std::vector<int32_t> h_dst_rank;          // per destination entry
   std::vector<uint64_t> expected_blocks;    // per rank and step
+  // Rank groups (counting per rank): group g holds the units whose lowest
+  // holding rank is g; rank_perm lists the units group by group (plan order
+  // within a group), group g is rank_perm[group_begin[g] .. group_begin[g+1]),
+  // and group_counts[g * num_ranks + r] is what it adds to rank r's counter.
+  std::vector<uint32_t> rank_perm;
+  std::vector<int64_t> group_begin;
+  std::vector<uint32_t> group_counts;
+  // The unit order of whole-step and offload-chunk launches when some
+  // units are slow (gathered row by row): those first, within each chunk's
+  // range; empty (plan order) otherwise.
+  std::vector<uint32_t> launch_perm;
   // per slot: rows and cols of the shard, whether the plan reads it
   // (non-empty, and of the local index in a shard-local plan) and whether a
   // tensor map is encoded for it (vec outputs, read shards)
@@ -212,8 +224,11 @@ struct Plan {
   bool prep_recorded[2] = {false, false};
   int32_t fail_chunk = -1;
   uint32_t* counters = nullptr;     // wt_plan_set_counters
-  uint32_t count_mode = 0;          // WT_COUNT_PER_LAUNCH or WT_COUNT_PER_BLOCK
+  uint32_t count_mode = 0;          // WT_COUNT_PER_LAUNCH or WT_COUNT_PER_RANK
   uint32_t* d_launch_counts = nullptr;   // [1 + chunks][ranks]: a step, then each chunk
+  const uint32_t* d_perm = nullptr;         // rank_perm on the device
+  const uint32_t* d_launch_perm = nullptr;  // launch_perm on the device, or NULL
+  const uint32_t* d_group_counts = nullptr; // group_counts on the device
   // testing hooks (wt_debug_stall_unit)
   int64_t stall_unit = -1;
   uint64_t wait_limit_ns = 0;        // 0: kDefaultTimeoutNs
@@ -234,7 +249,6 @@ constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;   // 2 s per wait
 cudaError_t prep_kernel_setup();
 // Launch over units [a.unit_begin, a.unit_end) with grid CTAs (at most one
 // per SM is resident).
-// With a.counters set, the kernel also signals every block's completion.
 cudaError_t launch_prepare(const PrepArgs& a, int grid, cudaStream_t s, bool debug);
 
 // counters.cu: counters[i] += counts[i] for i < n, queued on s after one

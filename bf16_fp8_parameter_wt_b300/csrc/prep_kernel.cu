@@ -76,7 +76,6 @@ struct SmemCtl {
   uint64_t empty[kStages];               // consumers -> producer
   float wmax[kGroups][2][kGroupWarps];   // per-warp block amax, double-buffered
   int abort_flag;
-  uint32_t stored[kGroups];              // units whose stores each group has issued
   uint8_t skew[kStages][kTile];          // unaligned rows: offset of the row in its slot
 };
 constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kStageStride + sizeof(SmemCtl);
@@ -101,10 +100,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
       : "r"(bar), "r"(parity)
       : "memory");
   return ok != 0;
-}
-
-__device__ __forceinline__ void red_release_cta_add(uint32_t* p, uint32_t v) {
-  asm volatile("red.release.cta.shared::cta.add.u32 [%0], %1;" ::"r"(smem_u32(p)), "r"(v) : "memory");
 }
 
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
@@ -236,9 +231,11 @@ __device__ __forceinline__ Batch load_batch(const PrepArgs& a, bool dyn, int64_t
     bt.n = (int)(n_local <= bt.first ? 0 : n_local - bt.first >= kBatch ? kBatch : n_local - bt.first);
   }
   bt.word = 0;
-  if ((lane >> 3) < bt.n)
-    bt.word = ld_nc_u32(reinterpret_cast<const uint32_t*>(a.units + batch_unit(dyn, bt, lane >> 3, first)) +
-                        (lane & 7));
+  if ((lane >> 3) < bt.n) {
+    int64_t u = batch_unit(dyn, bt, lane >> 3, first);
+    if (a.perm) u = ld_nc_u32(a.perm + u);
+    bt.word = ld_nc_u32(reinterpret_cast<const uint32_t*>(a.units + u) + (lane & 7));
+  }
   return bt;
 }
 
@@ -338,7 +335,11 @@ __device__ void producer(const PrepArgs& a, bool dyn, SmemCtl& sm, uint32_t stag
       }
       // testing hook: leave this unit's stage unfilled, so that its
       // consumers' wait runs out
-      if (batch_unit(dyn, cur, j, first) == a.stall_unit) continue;
+      if (a.stall_unit >= 0) {
+        int64_t u = batch_unit(dyn, cur, j, first);
+        if (a.perm) u = ld_nc_u32(a.perm + u);
+        if (u == a.stall_unit) continue;
+      }
       const uint32_t flags = w[5] >> 16;
       const uint32_t dst = stage0 + (uint32_t)st * kStageStride;
       if (lane == 0) {
@@ -601,7 +602,7 @@ __device__ __noinline__ void store_bf16_general(const PrepArgs& a, const DevUnit
   }
 }
 
-template <bool kDebug, bool kSignal>
+template <bool kDebug>
 __device__ void consumer(const PrepArgs& a, SmemCtl& sm, uint8_t* stages, int g, int t) {
   const int lane = t & 31, wg = t >> 5;
   const int cc = t & 15;       // 16-byte column chunk
@@ -693,98 +694,16 @@ __device__ void consumer(const PrepArgs& a, SmemCtl& sm, uint8_t* stages, int g,
       store_bf16_general<kDebug>(a, m, dp0, tp, r0, cc);
       mbar_arrive(empty);
     }
-    if (kSignal) {
-      // every thread of the group has issued this unit's stores: publish it
-      // to the signal warp (the barrier orders the group's stores before the
-      // CTA-scope release)
-      bar_sync(bar_id, kGroupThreads);
-      if (t == 0) red_release_cta_add(&sm.stored[g], 1u);
-    }
   }
 }
 
-// ------------------------------------------------------------ signal warp ---
-// Completion counters (the receiver-side immediate counter of a one-sided
-// transfer engine, "RDMA point-to-point communication for LLM systems"):
-// after the stores of a unit are visible device-wide, add one to the
-// counter of every rank that holds the unit's block. Units finish in order
-// within each consumer group, so the group's count says which are done; one
-// device-scope fence covers every unit found done since the last one, and
-// consecutive units for the same rank are added together.
-__device__ __forceinline__ uint32_t ld_acquire_cta_u32(const uint32_t* p) {
-  uint32_t v;
-  asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(smem_u32(p)) : "memory");
-  return v;
-}
-
-__device__ __forceinline__ void add_counter(uint32_t* c, uint32_t n) {
-  asm volatile("red.relaxed.gpu.global.add.u32 [%0], %1;" ::"l"(c), "r"(n) : "memory");
-}
-
-__device__ __forceinline__ bool unit_done(uint32_t s0, uint32_t s1, int64_t k) {
-  return (uint64_t)((k % kGroups) == 0 ? s0 : s1) > (uint64_t)(k / kGroups);
-}
-
-__device__ void signal_warp(const PrepArgs& a, SmemCtl& sm, int64_t first, int64_t n_local) {
-  static_assert(kGroups == 2, "the done test reads two group counts");
-  int64_t k = 0;
-  int32_t run_rank = -1;
-  uint32_t run_count = 0;
-  while (k < n_local) {
-    uint32_t s0 = ld_acquire_cta_u32(&sm.stored[0]), s1 = ld_acquire_cta_u32(&sm.stored[1]);
-    if (!unit_done(s0, s1, k)) {
-      const uint64_t t0 = globaltimer();
-      for (uint32_t i = 1;; ++i) {
-        __nanosleep(128);
-        s0 = ld_acquire_cta_u32(&sm.stored[0]);
-        s1 = ld_acquire_cta_u32(&sm.stored[1]);
-        if (unit_done(s0, s1, k)) break;
-        if ((i & 15u) == 0 &&
-            (*reinterpret_cast<volatile int*>(&sm.abort_flag) || globaltimer() - t0 > a.timeout_ns)) {
-          give_up(a, sm);
-          return;
-        }
-      }
-    }
-    int64_t end = k + 1;
-    while (end < n_local && unit_done(s0, s1, end)) ++end;
-    asm volatile("fence.acq_rel.gpu;" ::: "memory");
-    for (; k < end; ++k) {
-      const int64_t u = first + k * (int64_t)gridDim.x;
-      const uint32_t* w = reinterpret_cast<const uint32_t*>(a.units + u);
-      DevUnit m;
-      m.bi = ld_nc_u32(w + 2);
-      m.bj = ld_nc_u32(w + 3);
-      m.cols = ld_nc_u32(w + 4);
-      m.shape = ld_nc_u32(w + 5);
-      m.num_dsts = ld_nc_u32(w + 6);
-      m.dst_begin = ld_nc_u32(w + 7);
-      const bool check = m.num_dsts > 1 && ((m.shape >> 16) & kUnitSliced);
-      for (uint32_t d = 0; d < m.num_dsts; ++d) {
-        if (check && !place(a, m, m.dst_begin + d, 0, 0).held) continue;
-        const int32_t rank = (int32_t)ld_nc_u32(a.dst_rank + m.dst_begin + d);
-        if (rank != run_rank) {
-          if (run_count) add_counter(a.counters + run_rank, run_count);
-          run_rank = rank;
-          run_count = 0;
-        }
-        ++run_count;
-      }
-    }
-    if (run_count) add_counter(a.counters + run_rank, run_count);
-    run_count = 0;
-  }
-}
-
-template <bool kDebug, bool kSignal>
-__global__ void __launch_bounds__(kSignal ? kCtaThreads + 32 : kCtaThreads, 1)
-    prep_kernel(const __grid_constant__ PrepArgs a) {
+template <bool kDebug>
+__global__ void __launch_bounds__(kCtaThreads, 1) prep_kernel(const __grid_constant__ PrepArgs a) {
   extern __shared__ unsigned char smem_raw[];
   uint8_t* stages = reinterpret_cast<uint8_t*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   SmemCtl& sm = *reinterpret_cast<SmemCtl*>(stages + (size_t)kStages * kStageStride);
   const int tid = threadIdx.x;
-  // static assignment (per-block counting, or no ticket): CTA b takes units
-  // first, first + grid, ...; the signal warp walks the same sequence
+  // without a ticket counter, CTA b takes units first, first + grid, ...
   const int64_t first = a.unit_begin + blockIdx.x;
   const int64_t n_local = first < a.unit_end ? (a.unit_end - first + gridDim.x - 1) / gridDim.x : 0;
   if (tid == 0) {
@@ -793,18 +712,14 @@ __global__ void __launch_bounds__(kSignal ? kCtaThreads + 32 : kCtaThreads, 1)
       mbar_init(smem_u32(&sm.empty[s]), kGroupThreads);
     }
     sm.abort_flag = 0;
-    for (int g = 0; g < kGroups; ++g) sm.stored[g] = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
-  if (tid >= kCtaThreads) {
-    if (tid == kCtaThreads) signal_warp(a, sm, first, n_local);   // kSignal only
-  } else if (tid >= kConsumerThreads) {
-    producer(a, !kSignal && a.ticket, sm, smem_u32(stages), first, n_local, tid & 31);
-  } else {
-    consumer<kDebug, kSignal>(a, sm, stages, tid / kGroupThreads, tid % kGroupThreads);
-  }
-  if (kSignal || !a.ticket) return;
+  if (tid >= kConsumerThreads)
+    producer(a, a.ticket != nullptr, sm, smem_u32(stages), first, n_local, tid & 31);
+  else
+    consumer<kDebug>(a, sm, stages, tid / kGroupThreads, tid % kGroupThreads);
+  if (!a.ticket) return;
   // the last CTA to finish resets the ticket counter for the next launch:
   // every CTA takes its last ticket before it counts itself done
   __syncthreads();
@@ -823,26 +738,16 @@ __global__ void __launch_bounds__(kSignal ? kCtaThreads + 32 : kCtaThreads, 1)
 cudaError_t prep_kernel_setup() {
   const auto attr = cudaFuncAttributeMaxDynamicSharedMemorySize;
   cudaError_t e;
-  if ((e = cudaFuncSetAttribute(prep_kernel<false, false>, attr, (int)kSmemBytes)) != cudaSuccess ||
-      (e = cudaFuncSetAttribute(prep_kernel<true, false>, attr, (int)kSmemBytes)) != cudaSuccess ||
-      (e = cudaFuncSetAttribute(prep_kernel<false, true>, attr, (int)kSmemBytes)) != cudaSuccess)
-    return e;
-  return cudaFuncSetAttribute(prep_kernel<true, true>, attr, (int)kSmemBytes);
+  if ((e = cudaFuncSetAttribute(prep_kernel<false>, attr, (int)kSmemBytes)) != cudaSuccess) return e;
+  return cudaFuncSetAttribute(prep_kernel<true>, attr, (int)kSmemBytes);
 }
 
 cudaError_t launch_prepare(const PrepArgs& a, int grid, cudaStream_t s, bool debug) {
   if (a.unit_end <= a.unit_begin) return cudaSuccess;
-  const int signal_threads = kCtaThreads + 32;
-  if (a.counters) {
-    if (debug)
-      prep_kernel<true, true><<<grid, signal_threads, kSmemBytes, s>>>(a);
-    else
-      prep_kernel<false, true><<<grid, signal_threads, kSmemBytes, s>>>(a);
-  } else if (debug) {
-    prep_kernel<true, false><<<grid, kCtaThreads, kSmemBytes, s>>>(a);
-  } else {
-    prep_kernel<false, false><<<grid, kCtaThreads, kSmemBytes, s>>>(a);
-  }
+  if (debug)
+    prep_kernel<true><<<grid, kCtaThreads, kSmemBytes, s>>>(a);
+  else
+    prep_kernel<false><<<grid, kCtaThreads, kSmemBytes, s>>>(a);
   return cudaGetLastError();
 }
 

@@ -276,7 +276,7 @@ def wt_quantize_tokens(x: int, tokens: int, hidden: int, x_ld: int, codes: int, 
 
 
 WT_COUNT_PER_LAUNCH = 0
-WT_COUNT_PER_BLOCK = 1
+WT_COUNT_PER_RANK = 1
 
 
 def wt_plan_set_counters(plan: int, counters: int, mode: int = WT_COUNT_PER_LAUNCH) -> None:

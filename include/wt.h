@@ -365,20 +365,24 @@ wt_status wt_debug_fail_offload_chunk(wt_plan* p, int32_t chunk);
  * waits until counter >= base + expected (modulo 2^32) with an acquire
  * load sees the rank's whole step. The pages' transfer engine counts the
  * immediates of one-sided writes the same way ("RDMA point-to-point
- * communication for LLM systems", ImmCounter).
- *   WT_COUNT_PER_LAUNCH: the counts of each kernel launch (a whole step,
- *     or one offload chunk, so ranks complete chunk by chunk) are added by
- *     a small stream-ordered kernel right after it. No cost to the step.
- *     After a launch whose waits gave up (WT_ERR_TIMEOUT), nothing is
- *     counted until wt_plan_check has reported and cleared the error.
- *   WT_COUNT_PER_BLOCK: blocks are counted inside the kernel as their
- *     stores complete, in any order, so a rank can finish before the
- *     launch does. Each count needs a device-scope release, which on B300
- *     costs about 12 % of the step's throughput.
+ * communication for LLM systems", ImmCounter). Counts are added by a small
+ * stream-ordered kernel after a preparation launch has ended, so the
+ * stores they announce are complete; the modes differ in how a step is cut
+ * into launches:
+ *   WT_COUNT_PER_LAUNCH: wt_prepare runs one launch and adds the whole
+ *     step's counts after it.
+ *   WT_COUNT_PER_RANK: wt_prepare runs one launch per rank group -- the
+ *     blocks whose lowest holding rank is g, for g = 0, 1, ... -- each
+ *     followed by its counts, so rank g's counter is complete when group g
+ *     ends, before the step does, and the ranks finish one after another
+ *     (a sender can start on rank 0 while later ranks are prepared).
+ * wt_prepare_offload adds counts after each chunk's launch in both modes.
+ * After a launch whose waits gave up (WT_ERR_TIMEOUT), nothing more is
+ * counted until wt_plan_check has reported and cleared the error.
  * Errors: WT_ERR_INVALID_ARGUMENT (NULL plan, host-only plan, unknown
  * mode), WT_ERR_ALIGNMENT. */
 #define WT_COUNT_PER_LAUNCH 0u
-#define WT_COUNT_PER_BLOCK 1u
+#define WT_COUNT_PER_RANK 1u
 wt_status wt_plan_set_counters(wt_plan* p, uint32_t* counters, uint32_t mode);
 
 /* Blocks that `rank` receives per step: the amount one step adds to its

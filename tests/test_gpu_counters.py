@@ -35,7 +35,7 @@ def _read(c, n):
     return [int(v) & 0xFFFFFFFF for v in c[:n].cpu().tolist()]
 
 
-MODES = [wt.WT_COUNT_PER_LAUNCH, wt.WT_COUNT_PER_BLOCK]
+MODES = [wt.WT_COUNT_PER_LAUNCH, wt.WT_COUNT_PER_RANK]
 
 
 @pytest.mark.parametrize("mode", MODES)
@@ -113,7 +113,7 @@ def test_offload_steps_signal_too(oracle_mod, mode):
 
 @pytest.mark.parametrize("mode", MODES)
 def test_a_stalled_step_leaves_its_block_uncounted(oracle_mod, mode):
-    """Per block, the stalled step's counts stay short of a step; per launch,
+    """Per rank, the stalled step's counts stay short of a step; per launch,
     the step counts nothing. Either way the next good step adds exactly one
     step's counts once wt_plan_check has reported the timeout."""
     w = kimi_k2_moe_layer(4)
@@ -137,4 +137,25 @@ def test_a_stalled_step_leaves_its_block_uncounted(oracle_mod, mode):
     run_gpu(w, shards, pools=pools, plan=plan)
     plan.check()
     assert [a - b for a, b in zip(_read(c, w.num_ranks), partial)] == expected
+    plan.close()
+
+
+def test_per_rank_counting_completes_the_ranks_in_order(oracle_mod):
+    """Counting per rank runs the step rank group by rank group: when a unit
+    of rank 2's group stalls, ranks 0 and 1 have already received their
+    whole step's count and the later ranks nothing."""
+    w = kimi_k2_moe_layer(4)                   # experts 0..3 on ranks 0..3
+    shards = make_shards(w, device="cuda:0")
+    plan = wt.Plan(w, device=0)
+    pools = device_pools(plan, w.num_ranks)
+    c = _counters(w.num_ranks)
+    plan.set_counters(c.data_ptr(), wt.WT_COUNT_PER_RANK)
+    expected = [plan.expected_count(r) for r in range(w.num_ranks)]
+    per_expert = (4096 // 128) * (7168 // 128) + (7168 // 128) * (2048 // 128)
+    wt.wt_debug_stall_unit(plan.handle, 2 * per_expert + 100, 50_000_000)   # expert 2's gate_up
+    run_gpu(w, shards, pools=pools, plan=plan)
+    with pytest.raises(wt.WTError):
+        plan.check()
+    assert _read(c, w.num_ranks) == expected[:2] + [0] * (w.num_ranks - 2)
+    wt.wt_debug_stall_unit(plan.handle, -1, 0)
     plan.close()

@@ -98,7 +98,7 @@ def test_each_local_plan_writes_its_own_blocks_from_its_own_shard(oracle_mod, sh
         assert torch.equal(union[r], full_mask[r]), f"rank {r}: union differs from the full plan"
 
 
-@pytest.mark.parametrize("mode", [wt.WT_COUNT_PER_LAUNCH, wt.WT_COUNT_PER_BLOCK])
+@pytest.mark.parametrize("mode", [wt.WT_COUNT_PER_LAUNCH, wt.WT_COUNT_PER_RANK])
 def test_local_plans_together_give_the_oracle_pools(oracle_mod, mode):
     w = kimi_k2_moe_layer(8)
     src = make_shards(w, device="cuda:0")

@@ -326,6 +326,20 @@ def edge_stress() -> Workload:
     return b.w
 
 
+def edge_narrow(copies: int = 8) -> Workload:
+    """Rows that are not 16-byte aligned, at a size larger than L2: `copies`
+    outputs shaped like the edge set's 7168x2050 FP8 matrix (4100-byte
+    rows, a 2-column last block column), 3 uneven shards each, one rank
+    per output, the edge set's value recipe (seed 1009). copies=1 is the
+    edge set's matrix alone (L2-resident)."""
+    vals = ValueRecipe("student_t3", 0.02, 1009, zero_tile_eighths=1,
+                       outlier_tile_eighths=1, outlier=3.0e4)
+    b = _Builder(f"edge_narrow_x{copies}", copies, 3, vals)
+    for i in range(copies):
+        b.output(f"A{i}", [b.param(f"A{i}", 7168, 2050)], True, (i,))
+    return b.w
+
+
 def shard_local_mix(shards: int = 4) -> Workload:
     """Cases for shard-local preparation, where every FSDP shard boundary
     falls on a multiple of 128 rows of its output: empty shards, a ragged
@@ -402,5 +416,7 @@ WORKLOADS = {
     "halo_mix": halo_mix,
     "kimi_k2_moe_layer": kimi_k2_moe_layer,
     "edge_stress": edge_stress,
+    "edge_narrow": edge_narrow,
+    "edge_narrow_1": lambda: edge_narrow(1),
     "offload_layer": offload_layer,
 }
