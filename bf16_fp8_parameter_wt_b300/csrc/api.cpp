@@ -69,9 +69,10 @@ void free_device(Plan& p) {
 }
 
 // Layout of a pointer-table block (identical on the device and in its
-// pinned staging buffer): shard pointers, their tensor maps, destinations.
+// pinned staging buffer): shard pointers, their tensor maps, destinations,
+// and per shard whether its map is a view map.
 struct DynLayout {
-  size_t shards = 0, tmaps = 0, dsts = 0, bytes = 0;
+  size_t shards = 0, tmaps = 0, dsts = 0, views = 0, bytes = 0;
 };
 
 DynLayout dyn_layout(const Plan& p) {
@@ -79,7 +80,8 @@ DynLayout dyn_layout(const Plan& p) {
   d.shards = 0;
   d.tmaps = align256(d.shards + (size_t)p.num_slots * sizeof(void*));
   d.dsts = align256(d.tmaps + (size_t)p.num_slots * kTmapBytes);
-  d.bytes = align256(d.dsts + (size_t)p.num_dst_entries * sizeof(DevDstPtr));
+  d.views = align256(d.dsts + (size_t)p.num_dst_entries * sizeof(DevDstPtr));
+  d.bytes = align256(d.views + (size_t)p.num_slots);
   return d;
 }
 
@@ -112,12 +114,11 @@ wt_status upload(Plan& p, int device) {
   auto take = [&](size_t bytes) { size_t o = off; off = align256(off + bytes); return o; };
   const size_t o_dyn = take(dl.bytes * kPtrSets);
   const size_t o_units = take(p.h_units.size() * sizeof(DevUnit));
+  const size_t o_units_rank = take(p.h_units.size() * sizeof(DevUnit));
   const size_t o_runs = take(p.h_runs.size() * sizeof(DevRun));
   const size_t o_geom = take(p.h_geom.size() * sizeof(DevDstGeom));
   const size_t o_bmap = take(p.h_blockmap.size() * sizeof(int32_t));
-  const size_t o_perm = take(p.rank_perm.size() * sizeof(uint32_t));
   const size_t o_gcounts = take(p.group_counts.size() * sizeof(uint32_t));
-  const size_t o_lperm = take(p.launch_perm.size() * sizeof(uint32_t));
   // per-rank block counts of a whole step and of each offload chunk
   std::vector<uint32_t> lc((1 + p.chunks.size()) * (size_t)p.num_ranks, 0);
   for (int32_t r = 0; r < p.num_ranks; ++r) lc[(size_t)r] = (uint32_t)p.expected_blocks[(size_t)r];
@@ -128,36 +129,46 @@ wt_status upload(Plan& p, int device) {
             (uint32_t)(((ds.rows + kTile - 1) / kTile) * ((ds.cols + kTile - 1) / kTile));
   const size_t o_lc = take(lc.size() * sizeof(uint32_t));
   const size_t o_err = take(sizeof(int32_t));
-  const size_t o_ticket = take(2 * sizeof(uint32_t));
+  const size_t o_ticket = take(2 * sizeof(uint32_t) * (1 + (size_t)p.num_ranks));
   const size_t o_offl_s = take(offload ? n_slots * sizeof(void*) : 0);
   const size_t o_offl_t = take(offload ? n_slots * kTmapBytes : 0);
+  const size_t o_offl_v = take(offload ? n_slots : 0);
   e = cudaMalloc(&p.d_tables, std::max<size_t>(off, 256));
   if (e != cudaSuccess) return alloc_fail("cudaMalloc of plan tables failed");
   char* base = static_cast<char*>(p.d_tables);
   auto put = [&](size_t o, const void* src, size_t bytes) {
     return bytes ? cudaMemcpy(base + o, src, bytes, cudaMemcpyHostToDevice) : cudaSuccess;
   };
+  // the unit table in launch order and in rank-group order
+  std::vector<DevUnit> ordered(p.h_units.size());
+  const std::vector<DevUnit>* launch_units = &p.h_units;
+  if (!p.launch_perm.empty()) {
+    for (size_t i = 0; i < ordered.size(); ++i) ordered[i] = p.h_units[p.launch_perm[i]];
+    launch_units = &ordered;
+  }
   if ((e = cudaMemset(base + o_dyn, 0, dl.bytes * kPtrSets)) != cudaSuccess ||
-      (e = put(o_units, p.h_units.data(), p.h_units.size() * sizeof(DevUnit))) != cudaSuccess ||
+      (e = put(o_units, launch_units->data(), p.h_units.size() * sizeof(DevUnit))) != cudaSuccess)
+    return cuda_fail(e, "uploading plan tables");
+  for (size_t i = 0; i < ordered.size(); ++i) ordered[i] = p.h_units[p.rank_perm[i]];
+  if ((e = put(o_units_rank, ordered.data(), ordered.size() * sizeof(DevUnit))) != cudaSuccess ||
       (e = put(o_runs, p.h_runs.data(), p.h_runs.size() * sizeof(DevRun))) != cudaSuccess ||
       (e = put(o_geom, p.h_geom.data(), p.h_geom.size() * sizeof(DevDstGeom))) != cudaSuccess ||
       (e = put(o_bmap, p.h_blockmap.data(), p.h_blockmap.size() * sizeof(int32_t))) != cudaSuccess ||
-      (e = put(o_perm, p.rank_perm.data(), p.rank_perm.size() * sizeof(uint32_t))) != cudaSuccess ||
       (e = put(o_gcounts, p.group_counts.data(), p.group_counts.size() * sizeof(uint32_t))) != cudaSuccess ||
-      (e = put(o_lperm, p.launch_perm.data(), p.launch_perm.size() * sizeof(uint32_t))) != cudaSuccess ||
       (e = put(o_lc, lc.data(), lc.size() * sizeof(uint32_t))) != cudaSuccess ||
       (e = cudaMemset(base + o_err, 0, sizeof(int32_t))) != cudaSuccess ||
-      (e = cudaMemset(base + o_ticket, 0, 2 * sizeof(uint32_t))) != cudaSuccess)
+      (e = cudaMemset(base + o_ticket, 0, 2 * sizeof(uint32_t) * (1 + (size_t)p.num_ranks))) != cudaSuccess)
     return cuda_fail(e, "uploading plan tables");
   p.dyn_bytes = dl.bytes;
   p.d_error = reinterpret_cast<int32_t*>(base + o_err);
-  p.args.units = reinterpret_cast<const DevUnit*>(base + o_units);
+  p.d_units_launch = reinterpret_cast<const DevUnit*>(base + o_units);
+  p.d_units_rank = reinterpret_cast<const DevUnit*>(base + o_units_rank);
+  p.args.units = p.d_units_launch;
   p.args.runs = reinterpret_cast<const DevRun*>(base + o_runs);
-  p.args.ticket = reinterpret_cast<uint32_t*>(base + o_ticket);
+  p.d_tickets = reinterpret_cast<uint32_t*>(base + o_ticket);
+  p.args.ticket = p.d_tickets;
   p.args.geom = reinterpret_cast<const DevDstGeom*>(base + o_geom);
-  p.d_perm = reinterpret_cast<const uint32_t*>(base + o_perm);
   p.d_group_counts = reinterpret_cast<const uint32_t*>(base + o_gcounts);
-  p.d_launch_perm = p.launch_perm.empty() ? nullptr : reinterpret_cast<const uint32_t*>(base + o_lperm);
   p.d_launch_counts = reinterpret_cast<uint32_t*>(base + o_lc);
   p.args.blockmap = reinterpret_cast<const int32_t*>(base + o_bmap);
   p.args.error_word = p.d_error;
@@ -201,14 +212,17 @@ wt_status upload(Plan& p, int device) {
         }
     }
     std::vector<unsigned char> maps(n_slots * kTmapBytes);
+    std::vector<uint8_t> views(n_slots, 0);
     if (n_slots) {
-      wt_status st = encode_tmaps(p, tbl.data(), maps.data());
+      wt_status st = encode_tmaps(p, tbl.data(), maps.data(), views.data());
       if (st != WT_OK) return st;
     }
     p.d_offload_shard_ptrs = reinterpret_cast<const uint16_t**>(base + o_offl_s);
     p.d_offload_tmaps = reinterpret_cast<unsigned char*>(base + o_offl_t);
+    p.d_offload_view_ok = reinterpret_cast<const uint8_t*>(base + o_offl_v);
     if ((e = put(o_offl_s, tbl.data(), n_slots * sizeof(void*))) != cudaSuccess ||
-        (e = put(o_offl_t, maps.data(), n_slots * kTmapBytes)) != cudaSuccess)
+        (e = put(o_offl_t, maps.data(), n_slots * kTmapBytes)) != cudaSuccess ||
+        (e = put(o_offl_v, views.data(), n_slots)) != cudaSuccess)
       return cuda_fail(e, "uploading offload tables");
     p.offload_tmaps_dirty = true;
   }
@@ -281,7 +295,8 @@ wt_status stage_pointers(Plan& p, const void* const* shards, void* const* pools,
   if (shards_changed) {
     ps.shards_valid = false;
     std::memcpy(h + dl.shards, shards, n_slots * sizeof(void*));
-    wt_status st = encode_tmaps(p, shards, reinterpret_cast<unsigned char*>(h + dl.tmaps));
+    wt_status st = encode_tmaps(p, shards, reinterpret_cast<unsigned char*>(h + dl.tmaps),
+                                reinterpret_cast<uint8_t*>(h + dl.views));
     if (st != WT_OK) return st;
     ps.tmaps_dirty = true;
   }
@@ -320,6 +335,7 @@ void bind_set(const Plan& p, const PtrSet& ps, PrepArgs& a) {
   a.shard_ptrs = reinterpret_cast<const uint16_t* const*>(ps.d_block + dl.shards);
   a.tmaps = ps.d_block + dl.tmaps;
   a.dst_ptrs = reinterpret_cast<const DevDstPtr*>(ps.d_block + dl.dsts);
+  a.view_ok = ps.d_block + dl.views;
 }
 
 // One persistent CTA per SM (each holds a 128 KiB shared-memory ring).
@@ -430,32 +446,39 @@ wt_status wt_prepare(wt_plan* h, const void* const* shard_ptrs, void* const* poo
   PtrSet& ps = p.sets[set];
   PrepArgs a = p.args;
   bind_set(p, ps, a);
-  a.stall_unit = p.stall_unit;
   a.timeout_ns = p.wait_limit_ns ? p.wait_limit_ns : kDefaultTimeoutNs;
   a.tmap_fence = ps.tmaps_dirty ? 1u : 0u;
   const bool debug = p.flags & WT_FLAG_DEBUG_CHECKS;
   if (p.counters && p.count_mode == WT_COUNT_PER_RANK) {
     // rank by rank: the units whose lowest holding rank is g, then their
-    // counts; after launch g, ranks 0..g have all their blocks
-    a.perm = p.d_perm;
+    // counts; after launch g, ranks 0..g have all their blocks. Every launch
+    // after the first may start while the one before drains (programmatic
+    // dependent launch: the groups touch disjoint bytes and each has its
+    // own ticket words); each count kernel first waits for its group's
+    // launch to complete.
+    a.units = p.d_units_rank;
+    a.stall_unit = p.stall_pos_rank;
+    bool first = true;
     for (int32_t g = 0; g < p.num_ranks; ++g) {
       a.unit_begin = p.group_begin[(size_t)g];
       a.unit_end = p.group_begin[(size_t)g + 1];
       if (a.unit_end == a.unit_begin) continue;
-      if ((e = launch_prepare(a, grid_for(p, a.unit_end - a.unit_begin), s, debug)) != cudaSuccess)
+      a.ticket = p.d_tickets + 2 * (1 + (size_t)g);
+      if ((e = launch_prepare(a, grid_for(p, a.unit_end - a.unit_begin), s, debug, !first)) != cudaSuccess)
         return cuda_fail(e, "preparation kernel launch");
+      first = false;
       if ((e = launch_add_counts(p.counters, p.d_group_counts + (size_t)g * (size_t)p.num_ranks, p.num_ranks,
-                                 p.d_error, s)) != cudaSuccess)
+                                 p.d_error, s, true)) != cudaSuccess)
         return cuda_fail(e, "completion count launch");
     }
   } else {
-    a.perm = p.d_launch_perm;
+    a.stall_unit = p.stall_pos_launch;
     a.unit_begin = 0;
     a.unit_end = p.num_units;
-    e = launch_prepare(a, grid_for(p, p.num_units), s, debug);
+    e = launch_prepare(a, grid_for(p, p.num_units), s, debug, false);
     if (e != cudaSuccess) return cuda_fail(e, "preparation kernel launch");
     if (p.counters &&
-        (e = launch_add_counts(p.counters, p.d_launch_counts, p.num_ranks, p.d_error, s)) != cudaSuccess)
+        (e = launch_add_counts(p.counters, p.d_launch_counts, p.num_ranks, p.d_error, s, false)) != cudaSuccess)
       return cuda_fail(e, "completion count launch");
   }
   if (capturing) return WT_OK;         // the graph's replays are the caller's to track
@@ -488,10 +511,10 @@ wt_status wt_prepare_offload(wt_plan* h, const void* host_image, void* const* po
   PrepArgs a = p.args;
   bind_set(p, p.sets[set], a);
   a.shard_ptrs = p.d_offload_shard_ptrs;
+  a.view_ok = p.d_offload_view_ok;
   a.tmaps = p.d_offload_tmaps;
-  a.stall_unit = p.stall_unit;
+  a.stall_unit = p.stall_pos_launch;
   a.timeout_ns = p.wait_limit_ns ? p.wait_limit_ns : kDefaultTimeoutNs;
-  a.perm = p.d_launch_perm;          // keeps every chunk's unit range
   const char* host = static_cast<const char*>(host_image);
   auto drain = [&](wt_status s_, const std::string& msg) {
     cudaStreamSynchronize(cs);
@@ -518,12 +541,12 @@ wt_status wt_prepare_offload(wt_plan* h, const void* host_image, void* const* po
     a.unit_end = c.unit_end;
     a.tmap_fence = p.offload_tmaps_dirty ? 1u : 0u;
     if ((e = launch_prepare(a, grid_for(p, c.unit_end - c.unit_begin), ks,
-                            p.flags & WT_FLAG_DEBUG_CHECKS)) != cudaSuccess)
+                            p.flags & WT_FLAG_DEBUG_CHECKS, false)) != cudaSuccess)
       return drain(WT_ERR_CUDA, std::string("preparation kernel launch: ") + cudaGetErrorString(e));
     if (c.unit_end > c.unit_begin) p.offload_tmaps_dirty = false;
     if (p.counters &&
         (e = launch_add_counts(p.counters, p.d_launch_counts + (1 + i) * (size_t)p.num_ranks, p.num_ranks,
-                               p.d_error, ks)) != cudaSuccess)
+                               p.d_error, ks, false)) != cudaSuccess)
       return drain(WT_ERR_CUDA, std::string("completion count launch: ") + cudaGetErrorString(e));
     if ((e = cudaEventRecord(p.prep_done[b], ks)) != cudaSuccess)
       return drain(WT_ERR_CUDA, std::string("cudaEventRecord: ") + cudaGetErrorString(e));
@@ -580,8 +603,14 @@ wt_status wt_plan_expected_count(const wt_plan* h, int32_t rank, uint64_t* count
 wt_status wt_debug_stall_unit(wt_plan* h, int64_t unit, uint64_t wait_limit_ns) {
   if (!h) return fail(WT_ERR_INVALID_ARGUMENT, "plan is NULL");
   if (unit < -1 || unit >= h->p.num_units) return fail(WT_ERR_INVALID_ARGUMENT, "unit out of range");
-  h->p.stall_unit = unit;
-  h->p.wait_limit_ns = wait_limit_ns;
+  Plan& p = h->p;
+  p.stall_unit = unit;
+  p.stall_pos_launch = p.stall_pos_rank = -1;
+  for (int64_t i = 0; unit >= 0 && i < p.num_units; ++i) {
+    if ((p.launch_perm.empty() ? i : (int64_t)p.launch_perm[(size_t)i]) == unit) p.stall_pos_launch = i;
+    if ((int64_t)p.rank_perm[(size_t)i] == unit) p.stall_pos_rank = i;
+  }
+  p.wait_limit_ns = wait_limit_ns;
   return WT_OK;
 }
 

@@ -50,6 +50,11 @@ __global__ void __launch_bounds__(256) wait_counters_kernel(const __grid_constan
 
 __global__ void __launch_bounds__(256) add_counts_kernel(uint32_t* counters, const uint32_t* counts, int32_t n,
                                                         const int32_t* error_word) {
+  // launched as a programmatic dependent: let the next launch begin, then
+  // wait until the preparation before this kernel has completed and its
+  // stores are visible (returns at once after an ordinary launch)
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   // a launch whose waits gave up stored only part of its blocks: count none
   if (error_word && (*reinterpret_cast<const volatile int32_t*>(error_word) & kErrTimeout)) return;
   asm volatile("fence.acq_rel.gpu;" ::: "memory");
@@ -62,10 +67,18 @@ __global__ void __launch_bounds__(256) add_counts_kernel(uint32_t* counters, con
 }  // namespace
 
 cudaError_t launch_add_counts(uint32_t* counters, const uint32_t* counts, int32_t n, const int32_t* error_word,
-                              cudaStream_t s) {
+                              cudaStream_t s, bool pdl) {
   if (n <= 0) return cudaSuccess;
-  add_counts_kernel<<<1, 256, 0, s>>>(counters, counts, n, error_word);
-  return cudaGetLastError();
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(1);
+  cfg.blockDim = dim3(256);
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, add_counts_kernel, counters, counts, n, error_word);
 }
 
 }  // namespace wt

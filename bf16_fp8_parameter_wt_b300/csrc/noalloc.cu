@@ -100,7 +100,8 @@ extern "C" wt_status wt_prepare_noalloc(const wt_plan_desc* desc, const void* co
   const size_t o_shards = 0;
   const size_t o_tmaps = up256(o_shards + n_slots * sizeof(void*));
   const size_t o_dsts = up256(o_tmaps + n_slots * kTmapBytes);
-  const size_t o_units = up256(o_dsts + (size_t)p.num_dst_entries * sizeof(DevDstPtr));
+  const size_t o_views = up256(o_dsts + (size_t)p.num_dst_entries * sizeof(DevDstPtr));
+  const size_t o_units = up256(o_views + n_slots);
   const size_t o_runs = up256(o_units + p.h_units.size() * sizeof(DevUnit));
   const size_t o_geom = up256(o_runs + p.h_runs.size() * sizeof(DevRun));
   const size_t o_bmap = up256(o_geom + p.h_geom.size() * sizeof(DevDstGeom));
@@ -139,7 +140,7 @@ extern "C" wt_status wt_prepare_noalloc(const wt_plan_desc* desc, const void* co
   unsigned char* h = img.data();
   if (n_slots) {
     std::memcpy(h + o_shards, shard_ptrs, n_slots * sizeof(void*));
-    if ((st = encode_tmaps(p, shard_ptrs, h + o_tmaps)) != WT_OK) return st;
+    if ((st = encode_tmaps(p, shard_ptrs, h + o_tmaps, h + o_views)) != WT_OK) return st;
   }
   DevDstPtr* dp = reinterpret_cast<DevDstPtr*>(h + o_dsts);
   for (const OutputInfo& oi : p.outputs)
@@ -171,10 +172,10 @@ extern "C" wt_status wt_prepare_noalloc(const wt_plan_desc* desc, const void* co
   PrepArgs a{};
   a.units = reinterpret_cast<const DevUnit*>(dbase + o_units);
   a.tmaps = reinterpret_cast<const unsigned char*>(dbase + o_tmaps);
+  a.view_ok = reinterpret_cast<const uint8_t*>(dbase + o_views);
   a.tmap_fence = 1;                    // the maps were just rewritten
   a.timeout_ns = g_wait_limit_ns ? g_wait_limit_ns : kDefaultTimeoutNs;
   a.stall_unit = g_stall_unit;
-  a.perm = nullptr;
   a.runs = reinterpret_cast<const DevRun*>(dbase + o_runs);
   a.shard_ptrs = reinterpret_cast<const uint16_t* const*>(dbase + o_shards);
   a.dst_ptrs = reinterpret_cast<const DevDstPtr*>(dbase + o_dsts);
@@ -185,7 +186,7 @@ extern "C" wt_status wt_prepare_noalloc(const wt_plan_desc* desc, const void* co
   a.error_word = reinterpret_cast<int32_t*>(dbase + kErrorOffset);
   a.ticket = reinterpret_cast<uint32_t*>(dbase + o_ticket);
   const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(p.num_units, g_sm_count[device]));
-  e = launch_prepare(a, grid, s, false);
+  e = launch_prepare(a, grid, s, false, false);
   if (e != cudaSuccess) return fail_na(WT_ERR_CUDA, std::string("preparation kernel launch: ") + cudaGetErrorString(e));
   return WT_OK;
 }

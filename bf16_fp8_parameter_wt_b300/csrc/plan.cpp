@@ -264,6 +264,9 @@ wt_status compile_plan(const wt_plan_desc* d, Plan* p) {
   p->slot_rows.assign(p->num_slots, 0);
   p->slot_cols.assign(p->num_slots, 0);
   p->slot_tmap.assign(p->num_slots, 0);
+  p->slot_view_k.assign(p->num_slots, 1);
+  // the element-path test flag keeps every unaligned row on the row-by-row path
+  const bool views = !(p->flags & WT_FLAG_FORCE_NARROW);
   p->slot_used.assign(p->num_slots, 0);
   p->slot_read_rows.assign(p->num_slots, 0);
   for (const auto& pi : p->params)
@@ -275,8 +278,18 @@ wt_status compile_plan(const wt_plan_desc* d, Plan* p) {
       p->slot_cols[pi.slot_base + s] = pi.cols;
       p->slot_read_rows[pi.slot_base + s] = own ? pi.shard_rows[s] : 0;
       // tensor maps only for whole shards: a one-shard block lies in a shard
-      // of this plan's own index
-      p->slot_tmap[pi.slot_base + s] = p->outputs[pi.output].vec && own && pi.shard_rows[s] > 0;
+      // of this plan's own index. Rows that are not 16-byte aligned get a
+      // view map (k consecutive rows per view row, see tmap.cpp) when the
+      // shard holds a whole view row and a view row is at least one box wide.
+      const auto& oi = p->outputs[pi.output];
+      const int32_t k = view_rows(pi.cols);
+      p->slot_view_k[pi.slot_base + s] = k;
+      if (own && pi.shard_rows[s] > 0) {
+        if (oi.vec)
+          p->slot_tmap[pi.slot_base + s] = 1;
+        else if (views && pi.shard_rows[s] >= k && (int64_t)k * pi.cols >= kViewBoxCols)
+          p->slot_tmap[pi.slot_base + s] = 2;
+      }
     }
   const bool halo = (p->flags & WT_FLAG_SHARD_HALO) != 0;
   p->bytes_read = p->bytes_written = 0;
@@ -351,7 +364,15 @@ wt_status compile_plan(const wt_plan_desc* d, Plan* p) {
       }
       // one shard and 16-byte rows: one 2-D tensor copy from that shard
       const bool tma = single && oi.vec;
-      const uint32_t f = flags | (single ? 0u : kUnitMulti) | (sliced ? kUnitSliced : 0u);
+      // unaligned rows from one shard whose view map holds all of the
+      // block's rows: k tensor copies instead of a bulk copy per row
+      bool view = false;
+      if (single && !oi.vec && p->slot_tmap[(size_t)run.slot] == 2) {
+        const int64_t k = p->slot_view_k[(size_t)run.slot];
+        const int64_t s0 = r0 - run.row0;
+        view = s0 + nrows <= (run.rows / k) * k;
+      }
+      const uint32_t f = flags | (single ? 0u : kUnitMulti) | (sliced ? kUnitSliced : 0u) | (view ? kUnitView : 0u);
       for (int64_t bj = 0; bj < tiles_n; ++bj) {
         const int64_t ncols = std::min<int64_t>(kTile, oi.cols - bj * kTile);
         DevUnit u;

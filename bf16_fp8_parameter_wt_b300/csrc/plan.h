@@ -16,12 +16,14 @@ namespace wt {
 
 constexpr int kTile = 128;        // block edge (rows and cols)
 constexpr int kTmapBytes = 128;   // one CUtensorMap
+constexpr int kViewBoxCols = 136; // columns of a view-map box: a block's 128 and 8 for the misalignment
 
 // DevUnit.shape flag bits (bits 16..23)
 constexpr uint32_t kUnitFp8 = 1u;    // e4m3 codes + scale, else BF16 bytes
 constexpr uint32_t kUnitVec = 2u;    // rows are 16-byte aligned: bulk-copy path, else element path
 constexpr uint32_t kUnitMulti = 4u;  // block rows come from more than one shard
 constexpr uint32_t kUnitSliced = 8u; // some destination of the output takes a slice
+constexpr uint32_t kUnitView = 16u;  // unaligned rows from one shard, inside its view map (see tmap.cpp)
 constexpr uint32_t kUnitEnd = 0x80u; // in the kernel only: a stage that ends the CTA's units
 
 // Error word bits set by the kernel
@@ -83,6 +85,7 @@ struct PrepArgs {
   const DevRun* runs;
   const uint16_t* const* shard_ptrs;
   const unsigned char* tmaps;        // kTmapBytes per slot, 64-byte aligned
+  const uint8_t* view_ok;            // per slot: its map is a view map (unaligned rows)
   const DevDstPtr* dst_ptrs;
   const DevDstGeom* geom;            // per destination entry, like dst_ptrs
   const int32_t* blockmap;
@@ -95,9 +98,6 @@ struct PrepArgs {
   // next ticket (a batch of kBatch consecutive units) and the CTAs done.
   // NULL: units are assigned statically (CTA b takes b, b + grid, ...).
   uint32_t* ticket;
-  // NULL, or the launch runs units perm[unit_begin .. unit_end) (a rank
-  // group's units, see Plan::rank_perm)
-  const uint32_t* perm;
 };
 
 // Host-side copy of one param.
@@ -196,7 +196,8 @@ struct Plan {
   // tensor map is encoded for it (vec outputs, read shards)
   std::vector<int64_t> slot_rows, slot_cols;
   std::vector<int64_t> slot_read_rows;      // leading rows of the shard read
-  std::vector<uint8_t> slot_used, slot_tmap;
+  std::vector<uint8_t> slot_used, slot_tmap;   // slot_tmap: 0 none, 1 block map, 2 view map
+  std::vector<int32_t> slot_view_k;            // rows per view row of a view map
   int32_t local_shard = -1;                 // >= 0: shard-local plan
 
   // device side: one allocation for the static tables and kPtrSets
@@ -218,6 +219,7 @@ struct Plan {
   void* staging[2] = {nullptr, nullptr};
   const uint16_t** d_offload_shard_ptrs = nullptr;
   unsigned char* d_offload_tmaps = nullptr;
+  const uint8_t* d_offload_view_ok = nullptr;
   bool offload_tmaps_dirty = false;
   cudaEvent_t h2d_done[2] = {nullptr, nullptr};
   cudaEvent_t prep_done[2] = {nullptr, nullptr};
@@ -226,11 +228,15 @@ struct Plan {
   uint32_t* counters = nullptr;     // wt_plan_set_counters
   uint32_t count_mode = 0;          // WT_COUNT_PER_LAUNCH or WT_COUNT_PER_RANK
   uint32_t* d_launch_counts = nullptr;   // [1 + chunks][ranks]: a step, then each chunk
-  const uint32_t* d_perm = nullptr;         // rank_perm on the device
-  const uint32_t* d_launch_perm = nullptr;  // launch_perm on the device, or NULL
+  // the unit table in the order of whole-step and offload launches
+  // (launch_perm, or plan order), and in rank-group order (rank_perm)
+  const DevUnit* d_units_launch = nullptr;
+  const DevUnit* d_units_rank = nullptr;
+  uint32_t* d_tickets = nullptr;    // two words per launch of a step: [0] whole step, [1 + g] group g
   const uint32_t* d_group_counts = nullptr; // group_counts on the device
-  // testing hooks (wt_debug_stall_unit)
-  int64_t stall_unit = -1;
+  // testing hooks (wt_debug_stall_unit): the unit, and its position in
+  // the launch-order and rank-order tables
+  int64_t stall_unit = -1, stall_pos_launch = -1, stall_pos_rank = -1;
   uint64_t wait_limit_ns = 0;        // 0: kDefaultTimeoutNs
 };
 
@@ -239,23 +245,32 @@ wt_status compile_plan(const wt_plan_desc* d, Plan* p);   // host only
 void set_error(const std::string& msg);
 
 // tmap.cpp: the 2-D tensor map of every slot that has one (zeros for the
-// others), kTmapBytes each, into out (64-byte aligned).
-wt_status encode_tmaps(const Plan& p, const void* const* shards, unsigned char* out);
+// others), kTmapBytes each, into out (64-byte aligned), and per slot in
+// view_ok whether its map is a view map (a slot with slot_tmap == 2 whose
+// pointer is 16-byte aligned).
+wt_status encode_tmaps(const Plan& p, const void* const* shards, unsigned char* out, uint8_t* view_ok);
+// The rows per view row of an output with `cols` columns whose rows are
+// not 16-byte aligned: the smallest k with k * cols * 2 a multiple of 16.
+inline int32_t view_rows(int64_t cols) { return (cols & 1) ? 8 : (cols & 2) ? 4 : (cols & 4) ? 2 : 1; }
 
 // prep_kernel.cu
 constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;   // 2 s per wait
 // One-time per-device set-up of the kernel (shared-memory size); call with
 // the device current.
 cudaError_t prep_kernel_setup();
-// Launch over units [a.unit_begin, a.unit_end) with grid CTAs (at most one
-// per SM is resident).
-cudaError_t launch_prepare(const PrepArgs& a, int grid, cudaStream_t s, bool debug);
+// Launch over units [a.unit_begin, a.unit_end) of a.units with grid CTAs
+// (at most one per SM is resident). pdl: the launch may begin while the
+// kernel before it on s is still running (programmatic dependent launch);
+// only for work that reads nothing that kernel writes.
+cudaError_t launch_prepare(const PrepArgs& a, int grid, cudaStream_t s, bool debug, bool pdl);
 
 // counters.cu: counters[i] += counts[i] for i < n, queued on s after one
 // device-scope fence (everything before it on s is complete and visible);
-// nothing is added while error_word holds kErrTimeout.
+// nothing is added while error_word holds kErrTimeout. pdl: launched as a
+// programmatic dependent of the kernel before it, which it waits for (and
+// lets the kernel after it begin at once).
 cudaError_t launch_add_counts(uint32_t* counters, const uint32_t* counts, int32_t n, const int32_t* error_word,
-                              cudaStream_t s);
+                              cudaStream_t s, bool pdl);
 
 }  // namespace wt
 

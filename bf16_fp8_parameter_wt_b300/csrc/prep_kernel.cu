@@ -76,7 +76,7 @@ struct SmemCtl {
   uint64_t empty[kStages];               // consumers -> producer
   float wmax[kGroups][2][kGroupWarps];   // per-warp block amax, double-buffered
   int abort_flag;
-  uint8_t skew[kStages][kTile];          // unaligned rows: offset of the row in its slot
+  uint16_t roff[kStages][kTile];         // unaligned rows: byte offset of each row in the stage
 };
 constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kStageStride + sizeof(SmemCtl);
 static_assert(kSmemBytes <= 227 * 1024, "shared memory");
@@ -231,22 +231,20 @@ __device__ __forceinline__ Batch load_batch(const PrepArgs& a, bool dyn, int64_t
     bt.n = (int)(n_local <= bt.first ? 0 : n_local - bt.first >= kBatch ? kBatch : n_local - bt.first);
   }
   bt.word = 0;
-  if ((lane >> 3) < bt.n) {
-    int64_t u = batch_unit(dyn, bt, lane >> 3, first);
-    if (a.perm) u = ld_nc_u32(a.perm + u);
-    bt.word = ld_nc_u32(reinterpret_cast<const uint32_t*>(a.units + u) + (lane & 7));
-  }
+  if ((lane >> 3) < bt.n)
+    bt.word = ld_nc_u32(reinterpret_cast<const uint32_t*>(a.units + batch_unit(dyn, bt, lane >> 3, first)) +
+                        (lane & 7));
   return bt;
 }
 
-// Rows from several shards, or rows that are not 16-byte aligned: one bulk
-// copy per row (the full_tensor() row gather). A 16-byte-aligned row lands
-// at its place in the stage; any other row is copied as the 16-byte-aligned
-// span that holds it into its 272-byte slot, at offset skew = address % 16
-// (the span starts at most 15 bytes before the row and ends at most 15
-// after it; both ends lie in the 16-byte granules of the row's own first
-// and last bytes, so no page that the row does not touch is read), and the
-// consumers move it into place.
+// Rows from several shards, or rows that are not 16-byte aligned without a
+// view map: one bulk copy per row (the full_tensor() row gather). A
+// 16-byte-aligned row lands at its place in the stage; any other row is
+// copied as the 16-byte-aligned span that holds it into its 272-byte slot,
+// at offset address % 16 (the span starts at most 15 bytes before the row
+// and ends at most 15 after it; both ends lie in the 16-byte granules of
+// the row's own first and last bytes, so no page that the row does not
+// touch is read), and the consumers move it into place.
 __device__ __forceinline__ void load_rows(const PrepArgs& a, SmemCtl& sm, const uint32_t (&w)[8], int st,
                                           uint32_t dst, uint32_t full, uint64_t pol, int lane) {
   const int nrows = (int)(w[5] & 0xFFu) + 1;
@@ -271,7 +269,7 @@ __device__ __forceinline__ void load_rows(const PrepArgs& a, SmemCtl& sm, const 
       if (narrow) {
         src[i] = p & ~(uintptr_t)15;
         len[i] = (uint32_t)(((p + row_bytes + 15) & ~(uintptr_t)15) - src[i]);
-        sm.skew[st][r] = (uint8_t)(p & 15);
+        sm.roff[st][r] = (uint16_t)(r * kSlotBytes + (p & 15));
       } else {
         src[i] = p;
         len[i] = row_bytes;
@@ -280,7 +278,7 @@ __device__ __forceinline__ void load_rows(const PrepArgs& a, SmemCtl& sm, const 
     }
   }
   total = __reduce_add_sync(kFull, total);
-  __syncwarp();                 // the skews are written before the stage's arrival
+  __syncwarp();                 // the row offsets are written before the stage's arrival
   if (lane == 0) mbar_arrive_tx(full, total);
   __syncwarp();
   const uint32_t stride = narrow ? (uint32_t)kSlotBytes : (uint32_t)kRowBytes;
@@ -288,6 +286,36 @@ __device__ __forceinline__ void load_rows(const PrepArgs& a, SmemCtl& sm, const 
   for (int i = 0; i < kTile / 32; ++i)
     if (len[i]) bulk_load(dst + (uint32_t)(lane + 32 * i) * stride, reinterpret_cast<const void*>(src[i]),
                           len[i], full, pol);
+}
+
+// Rows that are not 16-byte aligned, all from one shard that has a view map
+// (see tmap.cpp): the block's rows fall into k residue classes, each one
+// box of 128 / k view rows by 136 columns, copied by one tensor copy into
+// consecutive 272-byte slots of the stage; the producer records where each
+// block row starts (slot and offset 0..7 elements) for the consumers.
+__device__ __forceinline__ void load_view(const PrepArgs& a, SmemCtl& sm, const uint32_t (&w)[8], const DevRun& rn,
+                                          int st, uint32_t dst, uint32_t full, uint64_t pol, int lane) {
+  const int64_t N = w[4];
+  const int k = (N & 1) ? 8 : (N & 2) ? 4 : (N & 4) ? 2 : 1;
+  const int per_box = kTile / k;
+  const int64_t s0 = (int64_t)w[1] - rn.row0;   // the block's first row in the shard
+  const int64_t col0 = (int64_t)w[3] * kTile;
+#pragma unroll
+  for (int i = 0; i < kTile / 32; ++i) {
+    const int r = lane + 32 * i;
+    const int j = r % k;
+    const int64_t x = ((s0 + j) % k) * N + col0;
+    sm.roff[st][r] = (uint16_t)(((j * per_box) + r / k) * kSlotBytes + 2 * (int)(x & 7));
+  }
+  __syncwarp();                 // the row offsets are written before the stage's arrival
+  if (lane == 0) mbar_arrive_tx(full, (uint32_t)(kTile * kSlotBytes));
+  __syncwarp();
+  if (lane < k) {
+    const unsigned char* map = a.tmaps + (size_t)rn.slot * kTmapBytes;
+    const int64_t x = ((s0 + lane) % k) * N + col0;
+    tma_load_2d(dst + (uint32_t)(lane * per_box * kSlotBytes), map, (int)(x & ~(int64_t)7), (int)((s0 + lane) / k),
+                full, pol);
+  }
 }
 
 // dyn: units come from the ticket counter, else the static sequence.
@@ -335,11 +363,7 @@ __device__ void producer(const PrepArgs& a, bool dyn, SmemCtl& sm, uint32_t stag
       }
       // testing hook: leave this unit's stage unfilled, so that its
       // consumers' wait runs out
-      if (a.stall_unit >= 0) {
-        int64_t u = batch_unit(dyn, cur, j, first);
-        if (a.perm) u = ld_nc_u32(a.perm + u);
-        if (u == a.stall_unit) continue;
-      }
+      if (batch_unit(dyn, cur, j, first) == a.stall_unit) continue;
       const uint32_t flags = w[5] >> 16;
       const uint32_t dst = stage0 + (uint32_t)st * kStageStride;
       if (lane == 0) {
@@ -355,6 +379,16 @@ __device__ void producer(const PrepArgs& a, bool dyn, SmemCtl& sm, uint32_t stag
           mbar_arrive_tx(full, kStageBytes);
           tma_load_2d(dst, map, (int)(w[3] * kTile), (int)w[1], full, pol);
         }
+      } else if (flags & kUnitView) {
+        const DevRun rn = a.runs[w[0]];
+        if (a.view_ok[rn.slot]) {
+          if (lane == 0 && a.tmap_fence && (int64_t)rn.slot != last_slot)
+            tmap_acquire(a.tmaps + (size_t)rn.slot * kTmapBytes);
+          last_slot = rn.slot;
+          load_view(a, sm, w, rn, st, dst, full, pol, lane);
+        } else {
+          load_rows(a, sm, w, st, dst, full, pol, lane);
+        }
       } else {
         load_rows(a, sm, w, st, dst, full, pol, lane);
       }
@@ -365,6 +399,9 @@ __device__ void producer(const PrepArgs& a, bool dyn, SmemCtl& sm, uint32_t stag
   // a ticket taken but not used (after an abort) must still have landed
   // before this CTA counts itself done: wait for the atomic's return value
   if (dyn) asm volatile("" ::"r"((uint32_t)next_idx) : "memory");
+  // this CTA takes no more units: a launch queued after this one as a
+  // programmatic dependent may start once every CTA has said so
+  if (lane == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   // one end marker per consumer group: an arrival with no copy
   for (int e = 0; ok && e < kGroups; ++e, ++k) {
     const int st = (int)(k % kStages);
@@ -440,12 +477,12 @@ __device__ __forceinline__ Place place(const PrepArgs& a, const DevUnit& m, uint
   return pl;
 }
 
-// The thread's 16-byte chunk cc of an unaligned row held in its slot at
-// offset skew (even: rows are 2-byte aligned): four 4-byte loads, or five
-// and a 16-bit funnel shift when the chunk starts 2 bytes past a word.
-__device__ __forceinline__ uint4 ld_skewed(const uint8_t* slot, int skew, int cc) {
-  const uint32_t* w = reinterpret_cast<const uint32_t*>(slot + ((skew + 16 * cc) & ~3));
-  if ((skew & 2) == 0) return make_uint4(w[0], w[1], w[2], w[3]);
+// The 16 bytes at stage offset `off` (even: rows are 2-byte aligned): four
+// 4-byte loads, or five and a 16-bit funnel shift when they start 2 bytes
+// past a word.
+__device__ __forceinline__ uint4 ld_skewed(const uint8_t* sp, int off) {
+  const uint32_t* w = reinterpret_cast<const uint32_t*>(sp + (off & ~3));
+  if ((off & 2) == 0) return make_uint4(w[0], w[1], w[2], w[3]);
   const uint32_t w4 = w[4];
   return make_uint4(__funnelshift_r(w[0], w[1], 16), __funnelshift_r(w[1], w[2], 16),
                     __funnelshift_r(w[2], w[3], 16), __funnelshift_r(w[3], w4, 16));
@@ -461,8 +498,9 @@ __device__ __forceinline__ uint4 keep_first(uint4 v, int valid) {
   return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
-// Rows that are not 16-byte aligned arrive in slots (see load_rows): read
-// the thread's chunks from them, zero what lies outside the block, and,
+// Rows that are not 16-byte aligned arrive in slots (see load_rows and
+// load_view): read the thread's chunks from them, zero what lies outside
+// the block, and,
 // once the whole group has read, write them back at their places in the
 // stage, where the general store routines read them again.
 __device__ __forceinline__ void realign_stage(const SmemCtl& sm, int st, uint8_t* sp, int nrows, int ncols,
@@ -472,7 +510,7 @@ __device__ __forceinline__ void realign_stage(const SmemCtl& sm, int st, uint8_t
   for (int j = 0; j < kRows; ++j) {
     const int r = r0 + kRowStride * j;
     v[j] = make_uint4(0, 0, 0, 0);
-    if (r < nrows && valid > 0) v[j] = keep_first(ld_skewed(sp + r * kSlotBytes, sm.skew[st][r], cc), valid);
+    if (r < nrows && valid > 0) v[j] = keep_first(ld_skewed(sp, sm.roff[st][r] + 16 * cc), valid);
   }
   bar_sync(bar_id, kGroupThreads);
 #pragma unroll
@@ -742,13 +780,19 @@ cudaError_t prep_kernel_setup() {
   return cudaFuncSetAttribute(prep_kernel<true>, attr, (int)kSmemBytes);
 }
 
-cudaError_t launch_prepare(const PrepArgs& a, int grid, cudaStream_t s, bool debug) {
+cudaError_t launch_prepare(const PrepArgs& a, int grid, cudaStream_t s, bool debug, bool pdl) {
   if (a.unit_end <= a.unit_begin) return cudaSuccess;
-  if (debug)
-    prep_kernel<true><<<grid, kCtaThreads, kSmemBytes, s>>>(a);
-  else
-    prep_kernel<false><<<grid, kCtaThreads, kSmemBytes, s>>>(a);
-  return cudaGetLastError();
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(kCtaThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return debug ? cudaLaunchKernelEx(&cfg, prep_kernel<true>, a) : cudaLaunchKernelEx(&cfg, prep_kernel<false>, a);
 }
 
 }  // namespace wt

@@ -214,3 +214,42 @@ def test_all_zero_plan_and_misuse_errors():
     plan.prepare(flat, [p.data_ptr() for p in pools])
     torch.cuda.synchronize()
     plan.close()
+
+
+def test_unaligned_rows_view_maps_and_fallbacks(oracle_mod):
+    """Rows that are not 16-byte aligned: N = 2050, 2052, 2049 and 141 (view
+    rows of 4, 2, 8 and 8 shard rows), shards whose row counts leave a
+    partial view row at the end, a 9-column output too narrow for a view
+    map, blocks spanning shards; then the same shards copied to addresses 2
+    bytes past a 16-byte boundary, which must take the row-by-row path."""
+    params = [Param("a", 700, 2050, (301, 399)), Param("b", 390, 2052, (390,)),
+              Param("c", 260, 2049, (130, 130)), Param("d", 300, 141, (300,)),
+              Param("e", 140, 9, (140,))]
+    outs = [Output("a", (0,), True, (0,)), Output("b", (1,), True, (1,)),
+            Output("c", (2,), False, (0,)), Output("d", (3,), True, (1,)),
+            Output("e", (4,), True, (0,))]
+    w = Workload("views", params, outs, 2, ValueRecipe("student_t3", 0.02, 91, zero_tile_eighths=1,
+                                                       outlier_tile_eighths=1, outlier=3.0e4))
+    shards = make_shards(w, device="cuda:0")
+    want = oracle_pools(oracle_mod, w, shards)
+    plan, pools = run_gpu(w, shards)
+    plan.check()
+    assert_pools_equal(pools, want)
+    plan.close()
+    # the same values at addresses 2 bytes past a 16-byte boundary
+    keep = []
+    moved = []
+    for per in shards:
+        row = []
+        for s in per:
+            buf = torch.empty(s.numel() + 16, dtype=torch.bfloat16, device="cuda:0")
+            t = buf[1:1 + s.numel()].view(s.shape)
+            t.copy_(s)
+            assert t.data_ptr() % 16 == 2
+            keep.append(buf)
+            row.append(t)
+        moved.append(row)
+    plan, pools = run_gpu(w, moved)
+    plan.check()
+    assert_pools_equal(pools, want)
+    plan.close()
