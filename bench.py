@@ -53,8 +53,8 @@ L2_BYTES = 126 * 10**6
 # from the ncu capture summarised in profiles/ (16 experts, scaled by the
 # blocks processed to the 385-expert layer); valid only for the kernel
 # source it was taken on.
-TRAFFIC = {"kernel_sha256": "9acb5d282c5b9c94e37d63ef7558f71736e5faa07d04b86b21edd34ad3f16794",
-           "bytes_per_launch": 50023547035, "experts": 385}
+TRAFFIC = {"kernel_sha256": "1a53501fb10b6671c25b11fe1159efec1f155f03631a2261d892b46b437ac11b",
+           "bytes_per_launch": 50035249302, "experts": 385}
 
 
 def kernel_sha() -> str:
@@ -835,7 +835,9 @@ def run_offload_stack(args, world, rank, local):
     st = plan.stats
     # the ranks on one host share its memory: fewer distinct images (the
     # host-to-device traffic stays that of 8 layers), never none
-    n_images = max(1, min(args.images, int(pinned_budget(world) // st["host_bytes"])))
+    budget = pinned_budget(world)
+    fit = args.images if budget == float("inf") else int(budget // max(1, st["host_bytes"]))
+    n_images = max(1, min(args.images, fit))
     images = []
     for i in range(n_images):
         wi = offload_layer(args.experts, seed=1005 + 100 * rank + i)
