@@ -64,7 +64,10 @@ typedef enum {
 #define WT_OFFSET_AUTO UINT64_MAX
 
 /* Plan flags. */
-#define WT_FLAG_FORCE_NARROW 0x1u /* use the element-wise path everywhere (testing) */
+/* Testing: treat every output's rows as not 16-byte aligned and copy them
+ * one row at a time (no tensor or view maps), the path that rows from
+ * several shards and unaligned shards take. */
+#define WT_FLAG_FORCE_NARROW 0x1u
 #define WT_FLAG_DEBUG_CHECKS 0x2u /* bounds-check every store; see wt_plan_check   */
 /* Shard-local plan (FSDP rank `local_shard` prepares the blocks its own
  * shards hold, with no exchange): see wt_plan_desc.local_shard. */

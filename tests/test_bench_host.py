@@ -42,3 +42,18 @@ def test_end_to_end_leg_fits_the_pinned_budget():
         assert p.stats["host_bytes"] <= full / 8
     assert len(sub.outputs) == 2 * (385 // 8)
     assert bench.e2e_subset(llama_dense(), [], 10 ** 12, 1.0)[2] is None   # only the MoE layer is cut
+
+
+def test_rank_groups_counts_the_launches_of_a_step_counted_per_rank():
+    """A step counted per rank is one launch per non-empty rank group (the
+    blocks whose lowest holding rank is g): the bench's launch count."""
+    import bench
+    from workloads import edge_stress, kimi_k2_moe_layer, llama_dense_tp4, tiny_dense, tp_slices_small
+    assert bench.rank_groups(kimi_k2_moe_layer()) == 8
+    assert bench.rank_groups(kimi_k2_moe_layer(3)) == 3
+    assert bench.rank_groups(tiny_dense()) == 2
+    assert bench.rank_groups(edge_stress()) == 3          # ranks 3 and 4 receive nothing
+    assert bench.rank_groups(llama_dense_tp4()) == 4
+    # every block there has a destination on rank 0 (a whole-tensor replica,
+    # or a row slice covering every row): one group
+    assert bench.rank_groups(tp_slices_small()) == 1
