@@ -10,29 +10,32 @@
 // shards). FP8 = e4m3 "fn", RNE, saturating; scale = amax / 448 as an IEEE
 // binary32 division, 1.0 for an all-zero block; code = e4m3(fl32(x / scale)).
 //
-// Structure (one persistent CTA per SM, units strided by the grid):
+// Structure (one persistent CTA per SM):
+//   - units (128x128 blocks) come in batches of four consecutive units of
+//     the schedule, taken from a per-launch ticket counter, so that SMs
+//     that run faster take more of them and every SM finishes within about
+//     one batch of the others; the last CTA to finish resets the counter.
 //   - a producer warp moves each unit's BF16 block into a ring of four
-//     32 KiB shared-memory stages with the tensor memory accelerator: one
-//     2-D tensor copy when all 128 rows come from one shard, one 1-D bulk
-//     copy per row when they come from several (the full_tensor() row
-//     gather), nothing when rows are not 16-byte aligned (the consumers
-//     then gather those elements themselves). Full/empty mbarriers order
-//     the ring; the producer runs up to four units ahead, so HBM reads
-//     stay in flight while the consumers compute.
+//     34 KiB shared-memory stages with the tensor memory accelerator: one
+//     2-D tensor copy when all 128 rows come from one shard and are 16-byte
+//     aligned; for rows that are not, k tensor copies through the shard's
+//     view map (k shard rows per view row, see tmap.cpp); otherwise one 1-D
+//     bulk copy per row (the full_tensor() row gather across shards, or
+//     unaligned rows without a view map). Full/empty mbarriers order the
+//     ring; the producer runs up to four units ahead, so HBM reads stay in
+//     flight while the consumers compute.
 //   - two consumer groups of four warps take alternate units. Thread t of a
 //     group owns the 16-byte column chunk t % 16 of the rows t / 16 + 8 j,
-//     j = 0..15 (with G threads per group: rows t / 16 + (G / 16) j): it
-//     loads them from shared memory (conflict-free, two full
-//     256-byte rows per warp instruction), reduces |x| with packed bf16x2
-//     abs-max, a warp shuffle and one named barrier, quantises from
-//     registers, releases the stage and stores full 128-byte code lines.
-//     Each HBM byte is read once. That straight-line path covers a whole
-//     block of 16-byte rows with one destination (every block of the big
-//     workloads); partial blocks, unaligned rows, several destinations,
-//     extreme scales and debug checks go through general routines that
-//     re-read the thread's rows from the stage before releasing it, so
-//     their code stays out of the hot path's registers.
-//
+//     j = 0..15: it loads them from shared memory (conflict-free, two full
+//     256-byte rows per warp instruction; unaligned rows are read out of
+//     their slots), reduces |x| with packed bf16x2 abs-max, a warp shuffle
+//     and one named barrier, quantises from registers, releases the stage
+//     and stores its chunks. Each HBM byte is read once. That straight-line
+//     path covers whole blocks of 16-byte rows and blocks of unaligned rows
+//     with one destination; partial blocks of 16-byte rows, several
+//     destinations, extreme scales and debug checks go through general
+//     routines that re-read the thread's rows from the stage before
+//     releasing it, so their code stays out of the hot path's registers.
 // Division: each code is E(fl32(x / s)), computed from r = RN(1/s) with
 // one exact correction step (codec.cuh).
 //
@@ -499,12 +502,10 @@ __device__ __forceinline__ uint4 keep_first(uint4 v, int valid) {
 }
 
 // Rows that are not 16-byte aligned arrive in slots (see load_rows and
-// load_view): read the thread's chunks from them, zero what lies outside
-// the block, and,
-// once the whole group has read, write them back at their places in the
-// stage, where the general store routines read them again.
-__device__ __forceinline__ void realign_stage(const SmemCtl& sm, int st, uint8_t* sp, int nrows, int ncols,
-                                              int r0, int cc, int bar_id, uint4 (&v)[kRows]) {
+// load_view): the thread's chunks, read from them, with what lies outside
+// the block zeroed.
+__device__ __forceinline__ void read_slots(const SmemCtl& sm, int st, const uint8_t* sp, int nrows, int ncols,
+                                           int r0, int cc, uint4 (&v)[kRows]) {
   const int valid = ncols - 8 * cc;
 #pragma unroll
   for (int j = 0; j < kRows; ++j) {
@@ -512,7 +513,12 @@ __device__ __forceinline__ void realign_stage(const SmemCtl& sm, int st, uint8_t
     v[j] = make_uint4(0, 0, 0, 0);
     if (r < nrows && valid > 0) v[j] = keep_first(ld_skewed(sp, sm.roff[st][r] + 16 * cc), valid);
   }
-  bar_sync(bar_id, kGroupThreads);
+}
+
+// The thread's chunks written back at their aligned places in the stage
+// (256-byte rows) for the general routines, once the whole group has read
+// the slots they overlap.
+__device__ __forceinline__ void write_back(uint8_t* sp, int r0, int cc, const uint4 (&v)[kRows]) {
 #pragma unroll
   for (int j = 0; j < kRows; ++j)
     *reinterpret_cast<uint4*>(sp + (r0 + kRowStride * j) * kRowBytes + cc * 16) = v[j];
@@ -670,7 +676,7 @@ __device__ void consumer(const PrepArgs& a, SmemCtl& sm, uint8_t* stages, int g,
     uint4 v[kRows];
     const uint8_t* tp = sp + r0 * kRowBytes + cc * 16;
     if (!vec) {
-      realign_stage(sm, st, sp, nrows, ncols, r0, cc, bar_id, v);
+      read_slots(sm, st, sp, nrows, ncols, r0, cc, v);
     } else if (whole) {
 #pragma unroll
       for (int j = 0; j < kRows; ++j) v[j] = *reinterpret_cast<const uint4*>(tp + j * kRowStride * kRowBytes);
@@ -683,8 +689,11 @@ __device__ void consumer(const PrepArgs& a, SmemCtl& sm, uint8_t* stages, int g,
       }
     }
     // the common case runs straight through: a whole block of 16-byte rows
-    // with one destination; everything else takes the general routines
+    // with one destination; rows that are not 16-byte aligned with one
+    // destination also store from registers, chunk by chunk with the widest
+    // stores their addresses allow; everything else takes the general routines
     const bool fast = !kDebug && whole && vec && m.num_dsts == 1 && pl0.held;
+    const bool narrow_fast = !kDebug && !vec && m.num_dsts == 1 && pl0.held;
     const uint32_t empty = smem_u32(&sm.empty[st]);
 
     if (flags & kUnitFp8) {
@@ -719,7 +728,21 @@ __device__ void consumer(const PrepArgs& a, SmemCtl& sm, uint8_t* stages, int g,
         uint8_t* row = dp0.data + pl0.off;
 #pragma unroll
         for (int j = 0; j < kRows; ++j) __stcs(reinterpret_cast<uint2*>(row + j * pl0.step), q[j]);
+      } else if (narrow_fast && se >= kMinScaleExp && se <= kMaxScaleExp) {
+        const float r = __frcp_rn(s);
+        uint2 q[kRows];
+#pragma unroll
+        for (int j = 0; j < kRows; ++j) q[j] = quant_chunk(v[j], s, r);
+        mbar_arrive(empty);                       // the codes are in registers
+        if (t == 0) dp0.scale[pl0.sidx] = s;
+        uint8_t* row = dp0.data + pl0.off;
+        const int valid = ncols - cc * 8;
+        if (valid > 0)
+#pragma unroll
+          for (int j = 0; j < kRows; ++j)
+            store_codes_bytes<false>(a, dp0, row + j * pl0.step, q[j], r0 + kRowStride * j < nrows, valid);
       } else {
+        if (!vec) write_back(sp, r0, cc, v);      // the slots were read before the amax barrier
         store_fp8_general<kDebug>(a, m, dp0, tp, s, t, r0, cc);
         mbar_arrive(empty);
       }
@@ -728,7 +751,19 @@ __device__ void consumer(const PrepArgs& a, SmemCtl& sm, uint8_t* stages, int g,
       uint8_t* row = dp0.data + 2 * pl0.off;
 #pragma unroll
       for (int j = 0; j < kRows; ++j) __stcs(reinterpret_cast<uint4*>(row + 2 * j * pl0.step), v[j]);
+    } else if (narrow_fast) {
+      mbar_arrive(empty);                         // the block is in registers
+      uint8_t* row = dp0.data + 2 * pl0.off;
+      const int valid = ncols - cc * 8;
+      if (valid > 0)
+#pragma unroll
+        for (int j = 0; j < kRows; ++j)
+          if (r0 + kRowStride * j < nrows) store_bf16_chunk<false>(a, dp0, row + 2 * j * pl0.step, v[j], valid);
     } else {
+      if (!vec) {
+        bar_sync(bar_id, kGroupThreads);          // every thread has read its slots
+        write_back(sp, r0, cc, v);
+      }
       store_bf16_general<kDebug>(a, m, dp0, tp, r0, cc);
       mbar_arrive(empty);
     }
