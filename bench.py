@@ -53,8 +53,8 @@ L2_BYTES = 126 * 10**6
 # from the ncu capture summarised in profiles/ (16 experts, scaled by the
 # blocks processed to the 385-expert layer); valid only for the kernel
 # source it was taken on.
-TRAFFIC = {"kernel_sha256": "1a53501fb10b6671c25b11fe1159efec1f155f03631a2261d892b46b437ac11b",
-           "bytes_per_launch": 50035249302, "experts": 385}
+TRAFFIC = {"kernel_sha256": "a08fffb0ba64448728f67bbc7739a5d9dc8b1f25c71ba51d317618c91560bed2",
+           "bytes_per_launch": 50034218272, "experts": 385}
 
 
 def kernel_sha() -> str:
