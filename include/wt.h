@@ -216,22 +216,31 @@ wt_status wt_plan_output_layout(const wt_plan* p, int32_t out, int32_t dst,
                                 uint64_t* scale_off);
 
 /* Byte offset of (param, shard) inside the packed pinned-host image used
- * by wt_prepare_offload. The image holds the params in the order their
+ * by wt_prepare_offload (the "host-to-device memcpy if FSDP offloads to
+ * CPU" stage, "Weight transfer for RL post-training in under 2 seconds",
+ * section "Task pipeline"). The image holds the params in the order their
  * outputs appear (parts in fusion order), each param's shards in order,
- * every shard starting at a 256-byte boundary. */
+ * every shard starting at a 256-byte boundary. Errors:
+ * WT_ERR_INVALID_ARGUMENT (NULL argument, index out of range). */
 wt_status wt_plan_shard_host_offset(const wt_plan* p, int32_t param,
                                     int32_t shard, uint64_t* off);
 
 /* How many leading rows of (param, shard) one step of this plan reads:
- * every row for a full plan; for a shard-local plan, every row of the
- * shards of its own index, the halo rows of the shards its blocks span
- * into (WT_FLAG_SHARD_HALO), 0 otherwise. A shard with 0 rows read may be
- * NULL in wt_prepare; one with r < shard_rows rows read needs only its
- * first r rows valid at the pointer passed (a halo buffer received from
- * the rank that holds the shard). */
+ * every row for a full plan; for a shard-local plan (the FSDP placement of
+ * "Weight transfer for RL post-training in under 2 seconds", section
+ * "DeviceMesh and mesh groups"), every row of the shards of its own index,
+ * the halo rows of the shards its blocks span into (WT_FLAG_SHARD_HALO),
+ * 0 otherwise. A shard with 0 rows read may be NULL in wt_prepare; one
+ * with r < shard_rows rows read needs only its first r rows valid at the
+ * pointer passed (a halo buffer received from the rank that holds the
+ * shard). Errors: WT_ERR_INVALID_ARGUMENT (NULL argument, index out of
+ * range). */
 wt_status wt_plan_shard_rows_read(const wt_plan* p, int32_t param, int32_t shard,
                                   int64_t* rows);
 
+/* Algorithmic sizes of one step of this plan (what a roofline divides by).
+ * No counterpart on the pages. Errors: WT_ERR_INVALID_ARGUMENT (NULL
+ * argument). */
 wt_status wt_plan_get_stats(const wt_plan* p, wt_plan_stats* stats);
 
 /* One step: run the preparation of every output on `stream` -- the
@@ -246,8 +255,10 @@ wt_status wt_plan_get_stats(const wt_plan* p, wt_plan_stats* stats);
  *   of wt_plan_desc.params and their shard_rows); each shard is a
  *   contiguous shard_rows x cols BF16 row-major block. A shard with 0 rows,
  *   or one that a shard-local plan does not read, may be NULL; of a halo
- *   shard only the rows read need be valid (wt_plan_shard_rows_read). Shards of outputs whose cols are a multiple of 8 must be
- *   16-byte aligned.
+ *   shard only the rows read need be valid (wt_plan_shard_rows_read).
+ *   Shards of outputs whose cols are a multiple of 8 must be 16-byte
+ *   aligned, the others 2-byte aligned (a 16-byte-aligned one is read
+ *   through tensor copies, any other row by row).
  * pools: num_ranks device pointers, each 16-byte aligned, holding at least
  *   wt_plan_pool_bytes bytes (NULL allowed for a 0-byte pool).
  * Shards and pools are borrowed: they must stay valid until the stream
