@@ -256,7 +256,6 @@ wt_status compile_plan(const wt_plan_desc* d, Plan* p) {
   p->h_runs.clear();
   p->h_geom.clear();
   p->h_blockmap.clear();
-  p->h_dst_rank.clear();
   p->expected_blocks.assign((size_t)p->num_ranks, 0);
   p->group_counts.assign((size_t)p->num_ranks * (size_t)p->num_ranks, 0);
   std::vector<int32_t> unit_group, held_ranks;
@@ -303,7 +302,6 @@ wt_status compile_plan(const wt_plan_desc* d, Plan* p) {
     const int64_t tiles_m = ceil_div(oi.rows, kTile), tiles_n_all = ceil_div(oi.cols, kTile);
     bool sliced = false;
     for (const DstInfo& ds : oi.dsts) {
-      p->h_dst_rank.push_back(ds.rank);
       DevDstGeom g;
       g.dim = ds.slice_dim;
       g.map_off = -1;

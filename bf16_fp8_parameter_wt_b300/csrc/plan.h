@@ -178,7 +178,6 @@ struct Plan {
   std::vector<DevRun> h_runs;
   std::vector<DevDstGeom> h_geom;           // per destination entry
   std::vector<int32_t> h_blockmap;
-  std::vector<int32_t> h_dst_rank;          // per destination entry
   std::vector<uint64_t> expected_blocks;    // per rank and step
   // Rank groups (counting per rank): group g holds the units whose lowest
   // holding rank is g; rank_perm lists the units group by group (plan order

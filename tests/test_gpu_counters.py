@@ -159,3 +159,33 @@ def test_per_rank_counting_completes_the_ranks_in_order(oracle_mod):
     assert _read(c, w.num_ranks) == expected[:2] + [0] * (w.num_ranks - 2)
     wt.wt_debug_stall_unit(plan.handle, -1, 0)
     plan.close()
+
+
+def test_per_rank_counting_replays_from_a_cuda_graph(oracle_mod):
+    """A step counted per rank (rank-group launches queued as programmatic
+    dependents, each followed by its count kernel) captured into a CUDA
+    graph: every replay writes the oracle's bytes and adds one step's counts."""
+    w = kimi_k2_moe_layer(4)
+    shards = make_shards(w, device="cuda:0")
+    want = oracle_pools(oracle_mod, w, shards)
+    plan = wt.Plan(w, device=0)
+    pools = device_pools(plan, w.num_ranks)
+    c = _counters(w.num_ranks)
+    plan.set_counters(c.data_ptr(), wt.WT_COUNT_PER_RANK)
+    expected = [plan.expected_count(r) for r in range(w.num_ranks)]
+    stream = torch.cuda.Stream()
+    sp, pp = plan.bind([s.data_ptr() for per in shards for s in per], [p.data_ptr() for p in pools])
+    plan.prepare(sp, pp, stream.cuda_stream)          # stages the pointers (one step counted)
+    stream.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        plan.prepare(sp, pp, stream.cuda_stream)
+    for step in (2, 3):
+        for p in pools:
+            p.fill_(CANARY)
+        torch.cuda.synchronize()
+        graph.replay()
+        torch.cuda.synchronize()
+        assert _read(c, w.num_ranks) == [step * e for e in expected]
+        assert_pools_equal(pools, want)
+    plan.close()

@@ -192,3 +192,43 @@ def test_noalloc_takes_no_device_memory():
         wt.wt_noalloc_check(stream)
     torch.cuda.synchronize()
     assert torch.cuda.mem_get_info(0)[0] == free0
+
+
+def test_noalloc_calls_from_two_host_threads_on_one_stream():
+    """Two host threads queue calls onto one stream at the same time (ctypes
+    releases the interpreter lock during the call): the library keeps each
+    call's table upload and kernel adjacent, so every call's pools hold the
+    bytes wt_prepare writes."""
+    import threading
+    w = tiny_dense()
+    shards = make_shards(w, device="cuda:0")
+    flat = [s.data_ptr() for per in shards for s in per]
+    stream = torch.cuda.current_stream().cuda_stream
+    plan = wt.Plan(w, device=0)
+    want = _pools(plan, w.num_ranks, CANARY)
+    plan.prepare(flat, [p.data_ptr() for p in want], stream)
+    torch.cuda.synchronize()
+    desc = wt.PlanDesc(w)
+    per_thread = [[_pools(plan, w.num_ranks, CANARY) for _ in range(12)] for _ in range(2)]
+    errors = []
+
+    def run(sets):
+        try:
+            for pools in sets:
+                wt.wt_prepare_noalloc(desc, flat, [p.data_ptr() for p in pools], stream)
+        except Exception as e:                 # reported below, in the test's thread
+            errors.append(e)
+
+    threads = [threading.Thread(target=run, args=(sets,)) for sets in per_thread]
+    for th in threads:
+        th.start()
+    for th in threads:
+        th.join()
+    assert not errors, errors
+    wt.wt_noalloc_check(stream)
+    torch.cuda.synchronize()
+    for sets in per_thread:
+        for pools in sets:
+            for r in range(w.num_ranks):
+                assert torch.equal(pools[r], want[r]), r
+    plan.close()
