@@ -129,3 +129,34 @@ def test_allocation_failure_is_reported_and_leaves_no_stale_error(oracle_mod):
     assert "offload staging" in str(ei.value)
     assert torch.cuda.mem_get_info(0)[0] >= free0 - (64 << 20)     # nothing left behind
     full_check(oracle_mod, tiny_dense())
+
+
+def test_offload_with_row_by_row_blocks_keeps_each_chunk_in_its_range(oracle_mod):
+    """Outputs with blocks gathered row by row (4100-byte rows, block rows
+    spanning shards, a 1-column norm) are handed out first within each
+    offload chunk; over several chunks, twice in a row, the pools equal the
+    oracle's."""
+    from workloads import Output, Param, ValueRecipe, Workload
+    params = [Param("a", 700, 2050, (301, 399)), Param("b", 300, 264, (1,) * 44 + (256,)),
+              Param("n", 512, 1, (100, 300, 112)), Param("c", 1000, 1024, (500, 500)),
+              Param("d", 640, 2049, (640,))]
+    outs = [Output("a", (0,), True, (0,)), Output("b", (1,), True, (1,)),
+            Output("n", (2,), False, (0,)), Output("c", (3,), True, (1,)),
+            Output("d", (4,), False, (0,))]
+    w = Workload("offload_slow_first", params, outs, 2,
+                 ValueRecipe("student_t3", 0.02, 93, zero_tile_eighths=1, outlier_tile_eighths=1,
+                             outlier=3.0e4))
+    shards = make_shards(w, device="cuda:0")
+    want = oracle_pools(oracle_mod, w, shards)
+    plan = wt.Plan(w, device=0, offload_chunk_bytes=2 << 20)
+    assert plan.stats["num_chunks"] >= 4
+    host = _host_image(plan, shards)
+    pools = device_pools(plan, w.num_ranks)
+    copy_s, comp_s = torch.cuda.Stream(), torch.cuda.Stream()
+    for _ in range(2):
+        for p in pools:
+            p.fill_(CANARY)
+        _offload(plan, host, pools, copy_s, comp_s)
+        plan.check(comp_s.cuda_stream)
+        assert_pools_equal(pools, want)
+    plan.close()

@@ -232,3 +232,19 @@ def test_noalloc_calls_from_two_host_threads_on_one_stream():
             for r in range(w.num_ranks):
                 assert torch.equal(pools[r], want[r]), r
     plan.close()
+
+
+def test_noalloc_equals_the_oracle(oracle_mod):
+    """The no-alloc call's pools against the CPU oracle directly (every
+    scheduled byte; padding left untouched)."""
+    from gpu_helpers import assert_pools_equal, oracle_pools
+    w = _small_shapes()
+    shards = make_shards(w, device="cuda:0")
+    flat = [s.data_ptr() if s.numel() else 0 for per in shards for s in per]
+    plan = wt.Plan(w, device=-1)
+    pools = _pools(plan, w.num_ranks, CANARY)
+    plan.close()
+    wt.wt_prepare_noalloc(wt.PlanDesc(w), flat, [p.data_ptr() for p in pools],
+                          torch.cuda.current_stream().cuda_stream)
+    wt.wt_noalloc_check(torch.cuda.current_stream().cuda_stream)
+    assert_pools_equal(pools, oracle_pools(oracle_mod, w, shards))
