@@ -11,7 +11,8 @@ import subprocess
 HERE = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
-SOURCES = ["api.cpp", "plan.cpp", "tmap.cpp", "prep_kernel.cu", "token_kernel.cu", "counters.cu", "noalloc.cu"]
+SOURCES = ["api.cpp", "plan.cpp", "tmap.cpp", "prep_kernel.cu", "token_kernel.cu", "counters.cu", "noalloc.cu",
+           "codec_sweep.cu"]
 HEADERS = ["plan.h", "codec.cuh"]
 LIB = os.path.join(HERE, "libwt.so")
 ARCH = "-gencode=arch=compute_103a,code=sm_103a"

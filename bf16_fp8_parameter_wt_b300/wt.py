@@ -31,7 +31,7 @@ EXPORTS = ["wt_plan_create", "wt_plan_pool_bytes", "wt_plan_output_layout",
            "wt_plan_shard_host_offset", "wt_plan_shard_rows_read", "wt_plan_get_stats", "wt_prepare", "wt_prepare_offload",
            "wt_plan_check", "wt_debug_fail_offload_chunk", "wt_debug_stall_unit", "wt_plan_destroy",
            "wt_prepare_noalloc", "wt_noalloc_check", "wt_debug_noalloc_stall_unit", "wt_quantize_tokens", "wt_plan_set_counters",
-           "wt_plan_expected_count", "wt_wait_counters",
+           "wt_plan_expected_count", "wt_wait_counters", "wt_debug_e4m3_encode",
            "wt_status_string", "wt_last_error"]
 
 
@@ -105,6 +105,7 @@ def lib() -> C.CDLL:
         L.wt_plan_set_counters.argtypes = [P, P, C.c_uint32]
         L.wt_plan_expected_count.argtypes = [P, C.c_int32, C.POINTER(C.c_uint64)]
         L.wt_wait_counters.argtypes = [P, C.c_int32, P, C.c_uint64, P, P]
+        L.wt_debug_e4m3_encode.argtypes = [C.c_uint32, C.c_uint64, P, P]
         L.wt_plan_destroy.argtypes = [P]
         L.wt_status_string.restype = C.c_char_p
         L.wt_status_string.argtypes = [C.c_int]
@@ -295,6 +296,12 @@ def wt_wait_counters(counters: int, targets: Sequence[int], limit_ns: int, statu
     t = (C.c_uint32 * max(1, len(targets)))(*[int(v) & 0xFFFFFFFF for v in targets])
     _check(lib().wt_wait_counters(counters or None, len(targets), t, limit_ns, status or None,
                                   stream or None))
+
+
+def wt_debug_e4m3_encode(first_bits: int, n: int, codes: int, stream: int = 0) -> None:
+    """The library's e4m3 convert applied to n consecutive fp32 bit patterns
+    (testing hook, see include/wt.h)."""
+    _check(lib().wt_debug_e4m3_encode(first_bits, n, codes or None, stream or None))
 
 
 def wt_debug_stall_unit(plan: int, unit: int, wait_limit_ns: int = 0) -> None:

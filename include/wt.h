@@ -426,6 +426,16 @@ wt_status wt_wait_counters(const uint32_t* counters, int32_t n, const uint32_t* 
  * unit = -1 restores normal operation. Errors: WT_ERR_INVALID_ARGUMENT. */
 wt_status wt_debug_stall_unit(wt_plan* p, int64_t unit, uint64_t wait_limit_ns);
 
+/* Testing hook for the e4m3 convert that every code of the library goes
+ * through (round to nearest even, saturating to +-448): it is applied on
+ * the current device, on `stream`, to the n fp32 values whose bit patterns
+ * are first_bits, first_bits + 1, ..., writing one code per value to
+ * `codes` (n bytes of device memory), so that a test can compare it with
+ * the CPU definition of the format over every fp32 value. No counterpart
+ * on the pages. Errors: WT_ERR_INVALID_ARGUMENT (codes NULL with n > 0,
+ * first_bits + n > 2^32), WT_ERR_CUDA. */
+wt_status wt_debug_e4m3_encode(uint32_t first_bits, uint64_t n, uint8_t* codes, void* stream);
+
 /* Synchronise the plan's device with the last stream it ran on, then free
  * the plan and everything it owns. NULL is accepted. The pages have no
  * counterpart (their schedule lives as long as the training job). Errors:
