@@ -19,7 +19,8 @@
  * Parity status per function (what pins each one in the tests):
  *   wo_e4m3_encode / wo_e4m3_decode : closed-form code table, a brute-force
  *       nearest-code search, exhaustive comparison with torch's e4m3fn cast
- *       over the whole non-saturating fp32 range.
+ *       over the whole non-saturating fp32 range, and with an independent
+ *       nearest-code search over all 2^32 fp32 bit patterns.
  *   wo_tile_scale, wo_quantize_element : numpy float32 division, the
  *       dequantisation error bound, exact-rational brute force.
  *   wo_layout, wo_dst_shape : closed-form pool sizes, disjointness, explicit
