@@ -233,3 +233,35 @@ def test_counter_calls_validate_arguments():
     assert L.wt_wait_counters(None, 1, t, 0, None, None) == 1
     assert L.wt_wait_counters(16, 1, None, 0, 16, None) == 1
     assert L.wt_wait_counters(18, 1, t, 0, 16, None) == 5         # misaligned counters
+
+
+def test_plan_owns_a_copy_of_its_descriptor(oracle_mod):
+    """wt_plan_create deep-copies the descriptor: after every array the
+    descriptor points to has been overwritten and freed, the plan's layout,
+    stats and errors are unchanged."""
+    import gc
+    w = llama_dense_tp4()
+    d, s, pools = oracle_mod.Model(w).layout()
+    desc = wt.PlanDesc(w)
+    h = wt.wt_plan_create(desc, -1)
+    try:
+        keep, params, outs = desc._keep
+        for arr in keep:
+            if isinstance(arr, ctypes.Array):
+                ctypes.memset(arr, 0xFF, ctypes.sizeof(arr))
+        ctypes.memset(params, 0xFF, ctypes.sizeof(params))
+        ctypes.memset(outs, 0xFF, ctypes.sizeof(outs))
+        del keep, params, outs, desc
+        gc.collect()
+        for r in range(w.num_ranks):
+            assert wt.wt_plan_pool_bytes(h, r) == pools[r]
+        for o, out in enumerate(w.outputs):
+            for k in range(len(out.dst_ranks)):
+                rr, dd, ss = wt.wt_plan_output_layout(h, o, k)
+                assert (rr, dd) == (out.dst_ranks[k], d[o][k])
+                if out.fp8:
+                    assert ss == s[o][k]
+        st = wt.wt_plan_get_stats(h)
+        assert st["bytes_read"] == w.bytes_read and st["bytes_written"] == w.bytes_written
+    finally:
+        wt.wt_plan_destroy(h)
