@@ -53,17 +53,17 @@ L2_BYTES = 126 * 10**6
 # from the ncu capture summarised in profiles/ (16 experts, scaled by the
 # blocks processed to the 385-expert layer); valid only for the kernel
 # source it was taken on.
-TRAFFIC = {"kernel_sha256": "a08fffb0ba64448728f67bbc7739a5d9dc8b1f25c71ba51d317618c91560bed2",
-           "bytes_per_launch": 50034218272, "experts": 385}
+TRAFFIC = {"kernel_sha256": "3f48660c3cec0adc021b2be45871991f743e5d5ae533e9d3a8e2db26cb2f670b",
+           "bytes_per_launch": 50021620880, "experts": 385}
 
 
 def kernel_sha() -> str:
     """Hash of the preparation kernel's device sources: the kernel, the
-    codec and the device part of plan.h (constants, table records, launch
-    arguments; the host-side plan structures after them do not reach the
-    kernel)."""
+    codec, the PTX primitives and the device part of plan.h (constants,
+    table records, launch arguments; the host-side plan structures after
+    them do not reach the kernel)."""
     h = hashlib.sha256()
-    for name in ("prep_kernel.cu", "codec.cuh", "plan.h"):
+    for name in ("prep_kernel.cu", "codec.cuh", "ptx.cuh", "plan.h"):
         with open(os.path.join(ROOT, "bf16_fp8_parameter_wt_b300", "csrc", name), "rb") as f:
             src = f.read()
         if name == "plan.h":
@@ -569,18 +569,21 @@ def main():
     graph_us = None
     if st["bytes_read"] <= L2_BYTES:
         # an L2-resident step is a latency figure: replay it from a CUDA graph
-        # so that the Python call around it is not timed
+        # so that the Python call around it is not timed, and 20 steps in one
+        # graph so that the host is not timed either
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph, stream=stream):
-            plan.prepare(shard_ptrs, pool_ptrs, sp)
-        for _ in range(3):
-            graph.replay()
+            for _ in range(20):
+                plan.prepare(shard_ptrs, pool_ptrs, sp)
         g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        g0.record(stream)
-        for _ in range(20):
+        with torch.cuda.stream(stream):          # replay() launches on the current stream
+            for _ in range(3):
+                graph.replay()
+            g0.record(stream)
             graph.replay()
-        g1.record(stream)
-        stream.synchronize()
+            g1.record(stream)
+            stream.synchronize()
+        plan.check(sp)
         graph_us = round(g0.elapsed_time(g1) * 1e3 / 20, 2)
 
     e2e = None
@@ -634,8 +637,9 @@ def main():
 def run_tokens(args, world, rank, local):
     """The 1 x 128 activation codec (wt_quantize_tokens) on a dispatch-shaped
     batch: --tokens x --hidden BF16 (Student-t(3) x 0.02), codes and scales
-    written to device buffers; the large default batch (1.9 GB) is larger
-    than L2, a 128-token batch gives the per-dispatch latency."""
+    written to device buffers, stages handed out from a ticket counter; the
+    large default batch (1.9 GB) is larger than L2, a 128-token batch gives
+    the per-dispatch latency."""
     import torch
     import bf16_fp8_parameter_wt_b300 as wt
     from bf16_fp8_parameter_wt_b300 import build as wt_build
@@ -652,10 +656,11 @@ def run_tokens(args, world, rank, local):
     codes = torch.empty(T, H, dtype=torch.uint8, device=dev)
     scales = torch.empty(T, G, dtype=torch.float32, device=dev)
     stream = torch.cuda.Stream(dev)
+    ticket = torch.zeros(2, dtype=torch.int32, device=dev)   # stage counter of the calls on `stream`
 
     def step():
         wt.wt_quantize_tokens(x.data_ptr(), T, H, H, codes.data_ptr(), scales.data_ptr(),
-                              stream.cuda_stream)
+                              stream.cuda_stream, ticket.data_ptr())
 
     for _ in range(args.warmup):
         step()
@@ -673,28 +678,34 @@ def run_tokens(args, world, rank, local):
         ends[i].record(stream)
     stream.synchronize()
     clk = clocks.stop()
+    wt.wt_tokens_check(stream.cuda_stream)       # no wait of the timed launches gave up
     per = [s_.elapsed_time(e_) for s_, e_ in zip(starts, ends)]
     ms = max_over_ranks(world, starts[0].elapsed_time(ends[-1]) / args.steps, dev)
-    # one dispatch-sized call (128 tokens), latency only: captured in a CUDA
-    # graph so that the replay times the kernel and its launch, not the
-    # Python call around it
+    # one dispatch-sized call (128 tokens), latency only: `reps` calls
+    # captured in one CUDA graph and replayed at once, so that the time is
+    # the GPU's per call (kernel and launch gap), not the host's rate of
+    # submitting graph launches
+    reps = 20
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph, stream=stream):
-        wt.wt_quantize_tokens(x.data_ptr(), 128, H, H, codes.data_ptr(), scales.data_ptr(),
-                              stream.cuda_stream)
-    for _ in range(3):
+        for _ in range(reps):
+            wt.wt_quantize_tokens(x.data_ptr(), 128, H, H, codes.data_ptr(), scales.data_ptr(),
+                                  stream.cuda_stream, ticket.data_ptr())
+    with torch.cuda.stream(stream):              # replay() launches on the current stream
+        for _ in range(3):
+            graph.replay()
+        small[0].record(stream)
         graph.replay()
-    stream.synchronize()
-    reps = 20
-    small[0].record(stream)
-    for _ in range(reps):
-        graph.replay()
-    small[1].record(stream)
-    stream.synchronize()
+        small[1].record(stream)
+        stream.synchronize()
+    wt.wt_tokens_check(stream.cuda_stream)
     bytes_in = 2 * T * H
     alg = bytes_in + T * H + 4 * T * G
     peak = measured_peaks().get("hbm_gbs") or 6400.0
     achieved = alg / (statistics.mean(per) * 1e-3) / 1e9
+    del graph, x, codes, scales
+    torch.cuda.empty_cache()
+    mix = mix_2to1_peak(dev, stream)
     line = {
         "metric": "wt_quantize_tokens GB/s (BF16 in), 1x128 e4m3 activation codec",
         "value": round(world * bytes_in / (ms * 1e-3) / 1e9, 2), "unit": "GB/s", "n_gpus": world,
@@ -706,8 +717,9 @@ def run_tokens(args, world, rank, local):
                          "inputs smaller than L2"},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "frac_of_8TBs_spec": round(achieved / SPEC_HBM_GBS, 4),
-                     "algorithmic_bytes_per_launch": alg, "kernel": "token_kernel",
-                     "launch_ms_median": round(statistics.median(per), 4)},
+                     "algorithmic_bytes_per_launch": alg, "kernel": "token_ring_kernel",
+                     "launch_ms_median": round(statistics.median(per), 4),
+                     "mix_2to1_peak": round(mix, 1), "frac_of_mix_2to1_peak": round(achieved / mix, 4)},
         "dispatch_128_tokens_us": round(small[0].elapsed_time(small[1]) * 1e3 / reps, 2),
         "clocks": clk, "gpu_launches": args.steps,
     }

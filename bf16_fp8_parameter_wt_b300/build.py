@@ -13,7 +13,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 SOURCES = ["api.cpp", "plan.cpp", "tmap.cpp", "prep_kernel.cu", "token_kernel.cu", "counters.cu", "noalloc.cu",
            "codec_sweep.cu"]
-HEADERS = ["plan.h", "codec.cuh"]
+HEADERS = ["plan.h", "codec.cuh", "ptx.cuh"]
 LIB = os.path.join(HERE, "libwt.so")
 ARCH = "-gencode=arch=compute_103a,code=sm_103a"
 

@@ -30,7 +30,8 @@ WT_FLAG_SHARD_HALO = 0x8
 EXPORTS = ["wt_plan_create", "wt_plan_pool_bytes", "wt_plan_output_layout",
            "wt_plan_shard_host_offset", "wt_plan_shard_rows_read", "wt_plan_get_stats", "wt_prepare", "wt_prepare_offload",
            "wt_plan_check", "wt_debug_fail_offload_chunk", "wt_debug_stall_unit", "wt_plan_destroy",
-           "wt_prepare_noalloc", "wt_noalloc_check", "wt_debug_noalloc_stall_unit", "wt_quantize_tokens", "wt_plan_set_counters",
+           "wt_prepare_noalloc", "wt_noalloc_check", "wt_debug_noalloc_stall_unit", "wt_quantize_tokens", "wt_tokens_check",
+           "wt_debug_tokens_stall_group", "wt_plan_set_counters",
            "wt_plan_expected_count", "wt_wait_counters", "wt_debug_e4m3_encode",
            "wt_status_string", "wt_last_error"]
 
@@ -101,7 +102,9 @@ def lib() -> C.CDLL:
         L.wt_plan_check.argtypes = [P, P]
         L.wt_debug_fail_offload_chunk.argtypes = [P, C.c_int32]
         L.wt_debug_stall_unit.argtypes = [P, C.c_int64, C.c_uint64]
-        L.wt_quantize_tokens.argtypes = [P, C.c_int64, C.c_int64, C.c_int64, P, P, P]
+        L.wt_quantize_tokens.argtypes = [P, C.c_int64, C.c_int64, C.c_int64, P, P, P, P]
+        L.wt_tokens_check.argtypes = [P]
+        L.wt_debug_tokens_stall_group.argtypes = [C.c_int64, C.c_uint64]
         L.wt_plan_set_counters.argtypes = [P, P, C.c_uint32]
         L.wt_plan_expected_count.argtypes = [P, C.c_int32, C.POINTER(C.c_uint64)]
         L.wt_wait_counters.argtypes = [P, C.c_int32, P, C.c_uint64, P, P]
@@ -270,10 +273,21 @@ def wt_debug_fail_offload_chunk(plan: int, chunk: int) -> None:
 
 
 def wt_quantize_tokens(x: int, tokens: int, hidden: int, x_ld: int, codes: int, scales: int,
-                       stream: int = 0) -> None:
-    """The 1 x 128 activation codec on device buffers (see include/wt.h)."""
+                       stream: int = 0, ticket: int = 0) -> None:
+    """The 1 x 128 activation codec on device buffers (see include/wt.h);
+    `ticket`: the address of two zeroed uint32 device words, or 0."""
     _check(lib().wt_quantize_tokens(x or None, tokens, hidden, x_ld, codes or None, scales or None,
-                                    stream or None))
+                                    ticket or None, stream or None))
+
+
+def wt_tokens_check(stream: int = 0) -> None:
+    """Synchronise `stream` and report (then clear) a wait that gave up in an
+    earlier wt_quantize_tokens kernel on the current device."""
+    _check(lib().wt_tokens_check(stream or None))
+
+
+def wt_debug_tokens_stall_group(group: int, wait_limit_ns: int = 0) -> None:
+    _check(lib().wt_debug_tokens_stall_group(group, wait_limit_ns))
 
 
 WT_COUNT_PER_LAUNCH = 0

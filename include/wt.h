@@ -350,11 +350,39 @@ wt_status wt_debug_noalloc_stall_unit(int64_t unit, uint64_t wait_limit_ns);
  * scales: tokens x ceil(hidden / 128) fp32, row-major; both caller-owned on
  * the same device. x 2-byte and scales 4-byte aligned; 16-byte-aligned x
  * with hidden and x_ld multiples of 8 (and 8-byte-aligned codes) take the
- * vector path. Asynchronous on `stream`, allocates nothing, no plan needed.
+ * vector path, and of those a contiguous batch (hidden a multiple of 128,
+ * x_ld == hidden) is streamed through shared memory by bulk copies, whose
+ * waits are bounded: one that gives up leaves that call's output
+ * incomplete and is reported by wt_tokens_check.
+ * ticket: NULL, or two uint32 words of device memory (4-byte aligned) that
+ * are zero before the first call that uses them. Large contiguous batches
+ * then hand their shared-memory stages to the SMs one at a time from this
+ * counter, so that SMs that are served faster take more (about 3 % faster
+ * on a 131072 x 7168 batch); every call leaves the words zero again, also
+ * when a wait gives up. Calls that share a ticket must not run at the same
+ * time (order them on one stream); NULL gives each SM a fixed share and
+ * has no such rule. Other shapes and small batches ignore it.
+ * Asynchronous on `stream`, allocates nothing, no plan needed.
  * Errors: WT_ERR_INVALID_ARGUMENT (hidden < 1, x_ld < hidden, NULL buffers,
  * more than 2^31 - 1 groups), WT_ERR_ALIGNMENT, WT_ERR_CUDA. */
 wt_status wt_quantize_tokens(const void* x, int64_t tokens, int64_t hidden, int64_t x_ld,
-                             void* codes, float* scales, void* stream);
+                             void* codes, float* scales, uint32_t* ticket, void* stream);
+
+/* Synchronise `stream`, then read and clear the error word that the
+ * kernels of earlier wt_quantize_tokens calls on the current device share:
+ * WT_ERR_TIMEOUT if a wait inside one of them gave up (that call's codes
+ * and scales are incomplete), WT_OK otherwise (also before any call on this
+ * device). No counterpart on the pages. Errors: WT_ERR_CUDA. */
+wt_status wt_tokens_check(void* stream);
+
+/* Testing hook of wt_quantize_tokens' bounded waits, for every later call
+ * of the process: the shared-memory stage that holds channel group `group`
+ * (token t's group g is t * ceil(hidden / 128) + g) is never copied, and
+ * every wait gives up after wait_limit_ns (0 = the default 2 s), so the
+ * kernel returns with WT_ERR_TIMEOUT recorded; group = -1 restores normal
+ * operation. Calls that are not streamed through shared memory ignore it.
+ * Errors: WT_ERR_INVALID_ARGUMENT (group < -1). */
+wt_status wt_debug_tokens_stall_group(int64_t group, uint64_t wait_limit_ns);
 
 /* Synchronise `stream`, then report what the kernels of earlier
  * wt_prepare* calls recorded, and clear it: WT_ERR_TIMEOUT if a wait inside

@@ -152,7 +152,7 @@ def test_null_arguments():
     L = wt.lib()
     assert L.wt_plan_create(None, -1, None) == 1
     assert L.wt_plan_pool_bytes(None, 0, None) == 1
-    assert L.wt_prepare(None, None, None, None) == 1
+    assert L.wt_prepare(None, None, None, None, None) == 1
     assert L.wt_plan_destroy(None) == 0
 
 
@@ -199,12 +199,14 @@ def test_tensor_parallel_blocks_have_one_destination():
 
 def test_token_codec_validates_arguments_before_touching_a_device():
     L = wt.lib()
-    assert L.wt_quantize_tokens(None, -1, 128, 128, None, None, None) == 1
-    assert L.wt_quantize_tokens(None, 4, 0, 128, None, None, None) == 1
-    assert L.wt_quantize_tokens(None, 4, 256, 128, None, None, None) == 1     # ld < hidden
-    assert L.wt_quantize_tokens(None, 4, 128, 128, None, None, None) == 1     # NULL buffers
-    assert L.wt_quantize_tokens(None, 0, 128, 128, None, None, None) == 0     # nothing to do
-    assert L.wt_quantize_tokens(2, 1 << 25, 1 << 13, 1 << 13, 16, 16, None) == 1  # > 2^31 groups
+    assert L.wt_quantize_tokens(None, -1, 128, 128, None, None, None, None) == 1
+    assert L.wt_quantize_tokens(None, 4, 0, 128, None, None, None, None) == 1
+    assert L.wt_quantize_tokens(None, 4, 256, 128, None, None, None, None) == 1     # ld < hidden
+    assert L.wt_quantize_tokens(None, 4, 128, 128, None, None, None, None) == 1     # NULL buffers
+    assert L.wt_quantize_tokens(None, 0, 128, 128, None, None, None, None) == 0     # nothing to do
+    assert L.wt_quantize_tokens(2, 1 << 25, 1 << 13, 1 << 13, 16, 16, None, None) == 1  # > 2^31 groups
+    align = wt.lib().wt_status_string
+    assert align(L.wt_quantize_tokens(2, 4, 128, 128, 16, 16, 6, None)) == b"WT_ERR_ALIGNMENT"  # ticket
 
 
 @pytest.mark.parametrize("make", [tiny_dense, llama_dense_tp4, tp_slices_small,
