@@ -463,8 +463,9 @@ wt_status wt_prepare(wt_plan* h, const void* const* shard_ptrs, void* const* poo
       a.unit_begin = p.group_begin[(size_t)g];
       a.unit_end = p.group_begin[(size_t)g + 1];
       if (a.unit_end == a.unit_begin) continue;
-      a.ticket = p.d_tickets + 2 * (1 + (size_t)g);
-      if ((e = launch_prepare(a, grid_for(p, a.unit_end - a.unit_begin), s, debug, !first)) != cudaSuccess)
+      const int grid = grid_for(p, a.unit_end - a.unit_begin);
+      a.ticket = tickets_for(p.d_tickets + 2 * (1 + (size_t)g), a.unit_end - a.unit_begin, grid);
+      if ((e = launch_prepare(a, grid, s, debug, !first)) != cudaSuccess)
         return cuda_fail(e, "preparation kernel launch");
       first = false;
       if ((e = launch_add_counts(p.counters, p.d_group_counts + (size_t)g * (size_t)p.num_ranks, p.num_ranks,
@@ -475,7 +476,9 @@ wt_status wt_prepare(wt_plan* h, const void* const* shard_ptrs, void* const* poo
     a.stall_unit = p.stall_pos_launch;
     a.unit_begin = 0;
     a.unit_end = p.num_units;
-    e = launch_prepare(a, grid_for(p, p.num_units), s, debug, false);
+    const int grid = grid_for(p, p.num_units);
+    a.ticket = tickets_for(p.d_tickets, p.num_units, grid);
+    e = launch_prepare(a, grid, s, debug, false);
     if (e != cudaSuccess) return cuda_fail(e, "preparation kernel launch");
     if (p.counters &&
         (e = launch_add_counts(p.counters, p.d_launch_counts, p.num_ranks, p.d_error, s, false)) != cudaSuccess)
@@ -540,8 +543,9 @@ wt_status wt_prepare_offload(wt_plan* h, const void* host_image, void* const* po
     a.unit_begin = c.unit_begin;
     a.unit_end = c.unit_end;
     a.tmap_fence = p.offload_tmaps_dirty ? 1u : 0u;
-    if ((e = launch_prepare(a, grid_for(p, c.unit_end - c.unit_begin), ks,
-                            p.flags & WT_FLAG_DEBUG_CHECKS, false)) != cudaSuccess)
+    const int grid = grid_for(p, c.unit_end - c.unit_begin);
+    a.ticket = tickets_for(p.d_tickets, c.unit_end - c.unit_begin, grid);
+    if ((e = launch_prepare(a, grid, ks, p.flags & WT_FLAG_DEBUG_CHECKS, false)) != cudaSuccess)
       return drain(WT_ERR_CUDA, std::string("preparation kernel launch: ") + cudaGetErrorString(e));
     if (c.unit_end > c.unit_begin) p.offload_tmaps_dirty = false;
     if (p.counters &&

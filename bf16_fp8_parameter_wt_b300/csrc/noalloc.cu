@@ -184,8 +184,8 @@ extern "C" wt_status wt_prepare_noalloc(const wt_plan_desc* desc, const void* co
   a.unit_begin = 0;
   a.unit_end = p.num_units;
   a.error_word = reinterpret_cast<int32_t*>(dbase + kErrorOffset);
-  a.ticket = reinterpret_cast<uint32_t*>(dbase + o_ticket);
   const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(p.num_units, g_sm_count[device]));
+  a.ticket = tickets_for(reinterpret_cast<uint32_t*>(dbase + o_ticket), p.num_units, grid);
   e = launch_prepare(a, grid, s, false, false);
   if (e != cudaSuccess) return fail_na(WT_ERR_CUDA, std::string("preparation kernel launch: ") + cudaGetErrorString(e));
   return WT_OK;

@@ -254,6 +254,17 @@ inline int32_t view_rows(int64_t cols) { return (cols & 1) ? 8 : (cols & 2) ? 4 
 
 // prep_kernel.cu
 constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;   // 2 s per wait
+
+// The ticket counter pays once CTAs take many units each. Each producer
+// takes its first three batches of four units at once, so in a launch with
+// fewer units per CTA the CTAs that start first would hold them all while
+// the rest had none (a 114-unit launch on 114 CTAs ran about ten times
+// longer than with one unit per CTA). Below this many units per CTA the
+// units are assigned statically: CTA b takes b, b + grid, ...
+constexpr int64_t kTicketMinUnitsPerCta = 48;
+inline uint32_t* tickets_for(uint32_t* ticket, int64_t units, int grid) {
+  return units >= kTicketMinUnitsPerCta * (int64_t)grid ? ticket : nullptr;
+}
 // One-time per-device set-up of the kernel (shared-memory size); call with
 // the device current.
 cudaError_t prep_kernel_setup();
