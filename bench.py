@@ -53,8 +53,8 @@ L2_BYTES = 126 * 10**6
 # from the ncu capture summarised in profiles/ (16 experts, scaled by the
 # blocks processed to the 385-expert layer); valid only for the kernel
 # source it was taken on.
-TRAFFIC = {"kernel_sha256": "3f48660c3cec0adc021b2be45871991f743e5d5ae533e9d3a8e2db26cb2f670b",
-           "bytes_per_launch": 50021620880, "experts": 385}
+TRAFFIC = {"kernel_sha256": "b74545c16da840cd3e3e88f261b0b76e733f80f5c554748701861753f1b1d707",
+           "bytes_per_launch": 50029567280, "experts": 385}
 
 
 def kernel_sha() -> str:

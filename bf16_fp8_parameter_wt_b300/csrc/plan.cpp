@@ -370,7 +370,12 @@ wt_status compile_plan(const wt_plan_desc* d, Plan* p) {
         const int64_t s0 = r0 - run.row0;
         view = s0 + nrows <= (run.rows / k) * k;
       }
-      const uint32_t f = flags | (single ? 0u : kUnitMulti) | (sliced ? kUnitSliced : 0u) | (view ? kUnitView : 0u);
+      // rows gathered one by one that the consumers load straight from the
+      // shards instead of through a bulk copy per row: 16-byte rows from
+      // several shards, and rows at most one 16-byte chunk wide
+      const bool direct = (!single && oi.vec) || (!oi.vec && oi.cols <= 8);
+      const uint32_t f = flags | (single ? 0u : kUnitMulti) | (sliced ? kUnitSliced : 0u) |
+                         (view ? kUnitView : 0u) | (direct ? kUnitDirect : 0u);
       for (int64_t bj = 0; bj < tiles_n; ++bj) {
         const int64_t ncols = std::min<int64_t>(kTile, oi.cols - bj * kTile);
         DevUnit u;

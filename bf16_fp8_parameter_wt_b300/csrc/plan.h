@@ -24,6 +24,10 @@ constexpr uint32_t kUnitVec = 2u;    // rows are 16-byte aligned: bulk-copy path
 constexpr uint32_t kUnitMulti = 4u;  // block rows come from more than one shard
 constexpr uint32_t kUnitSliced = 8u; // some destination of the output takes a slice
 constexpr uint32_t kUnitView = 16u;  // unaligned rows from one shard, inside its view map (see tmap.cpp)
+// The consumers load the block's rows themselves, from row addresses the
+// producer resolves: 16-byte rows from several shards, and rows one chunk
+// (at most 8 elements) wide. One copy per row cost about 5 us per block.
+constexpr uint32_t kUnitDirect = 32u;
 constexpr uint32_t kUnitEnd = 0x80u; // in the kernel only: a stage that ends the CTA's units
 
 // Error word bits set by the kernel
