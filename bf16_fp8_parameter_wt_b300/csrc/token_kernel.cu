@@ -9,25 +9,27 @@
 // two-step shuffle, and its scale and reciprocal are computed once per 32
 // elements of a lane.
 //
-// Large contiguous batches (hidden a multiple of 128, x_ld == hidden,
-// 16-byte aligned x) go through a TMA ring: the batch is one flat run of
-// groups, cut into stages of 128 groups (32 KiB; the last may be shorter).
+// Large batches of 16-byte-aligned rows with hidden a multiple of 128 go
+// through a TMA ring: the batch's groups, in token order, are cut into
+// stages of 128 groups (32 KiB; the last may be shorter), each copied with
+// one bulk copy when rows are contiguous (x_ld == hidden), else one per
+// token row it touches (rows of at least 32 groups).
 // A producer warp per CTA (one CTA per SM) copies stages into a ring of
 // shared-memory slots with cp.async.bulk and tells the consumers which
 // stage each slot holds; two consumer groups of twelve warps take alternate
 // slots, quantise from shared memory and store codes and scales straight
-// to global memory. With a caller's ticket counter the producers take
-// stages from it one at a time (SMs that are served faster take more; the
-// last CTA resets it), six slots deep; without one, CTA b takes stages b,
-// b + gridDim.x, ..., four slots deep (a deeper ring measured slower with
-// the fixed hand-out). Lane l of group j reads chunk 4 ((c + j) mod 4) +
+// to global memory. With a caller's ticket counter the producers of a
+// contiguous batch take stages from it one at a time, each ticket a stage
+// ahead (SMs that are served faster take more; the last CTA resets it), six
+// slots deep; otherwise CTA b takes stages b, b + gridDim.x, ..., four
+// slots deep (a deeper ring measured slower with the fixed hand-out). Lane l of group j reads chunk 4 ((c + j) mod 4) +
 // l % 4 at step c, so that the two groups in each 8-lane phase of a
 // 16-byte shared load fall in different bank halves. Every wait is
 // bounded; the role that gives up records kErrTimeout in the codec's error
 // word (wt_tokens_check).
 //
-// Smaller batches, and all other shapes (strided rows, hidden not a
-// multiple of 128, unaligned x), use a register-streaming kernel, which
+// Smaller batches, and all other shapes (hidden not a multiple of 128,
+// short strided rows, unaligned x), use a register-streaming kernel, which
 // starts faster than the ring fills: each lane loads its chunks of four
 // groups straight into registers (chunk c of lane l is chunk 4c + l % 4 of
 // the group, so each load instruction reads whole 64-byte runs and each
@@ -96,6 +98,8 @@ static_assert(kRingSmemBytes <= 227 * 1024, "shared memory");
 
 struct RingArgs {
   const uint16_t* x;
+  int64_t ld;                // row stride of x, elements (a multiple of 8)
+  uint32_t groups_per_token; // hidden / 128
   uint8_t* codes;
   float* scales;
   uint32_t* ticket;          // {next stage, CTAs done}, zero between launches; NULL: fixed hand-out
@@ -121,7 +125,8 @@ __device__ __forceinline__ uint4 lds_v4(uint32_t addr) {
 
 // One lane of the producer warp: ring entries 0, 1, ... are the CTA's
 // stages in the order it takes them, then one end marker per consumer
-// group.
+// group. With a ticket counter each stage's ticket is taken one stage
+// ahead, so that the atomic's round trip overlaps the wait for a slot.
 __device__ void ring_producer(const RingArgs& a, RingCtl& sm, uint8_t* stages) {
   const uint64_t pol = load_policy();
   const volatile int* abort_flag = &sm.abort_flag;
@@ -129,6 +134,7 @@ __device__ void ring_producer(const RingArgs& a, RingCtl& sm, uint8_t* stages) {
   uint32_t i = 0;                                    // ring entries filled so far
   int ends = 0;
   bool failed = false;
+  uint32_t next = a.ticket ? atomicAdd(a.ticket, 1u) : blockIdx.x;   // the first stage
   while (ends < kRingGroups) {
     const uint32_t slot = i % depth;
     if (i >= depth && !wait_bounded(smem_u32(&sm.empty[slot]), (i / depth - 1) & 1u, a.limit_ns, abort_flag)) {
@@ -138,8 +144,9 @@ __device__ void ring_producer(const RingArgs& a, RingCtl& sm, uint8_t* stages) {
     }
     uint32_t s = kStageEnd;
     if (!ends) {
-      s = a.ticket ? atomicAdd(a.ticket, 1u) : blockIdx.x + i * gridDim.x;
+      s = next;
       if (s >= a.num_stages) s = kStageEnd;
+      else next = a.ticket ? atomicAdd(a.ticket, 1u) : s + gridDim.x;
     }
     sm.stage_of[slot] = s;                           // published by the arrive below
     ++i;
@@ -150,10 +157,22 @@ __device__ void ring_producer(const RingArgs& a, RingCtl& sm, uint8_t* stages) {
     }
     if ((int64_t)s == a.stall_stage) continue;       // never armed: its consumers' wait runs out
     const uint32_t g0 = s * kRingStageGroups;
-    const uint32_t bytes = min((uint32_t)kRingStageGroups, a.num_groups - g0) * (uint32_t)(kTile * 2);
-    mbar_arrive_tx(smem_u32(&sm.full[slot]), bytes);
-    bulk_load(smem_u32(stages + (size_t)slot * kRingStageBytes), a.x + (size_t)g0 * kTile, bytes,
-              smem_u32(&sm.full[slot]), pol);
+    const uint32_t n = min((uint32_t)kRingStageGroups, a.num_groups - g0);
+    const uint32_t dst = smem_u32(stages + (size_t)slot * kRingStageBytes);
+    mbar_arrive_tx(smem_u32(&sm.full[slot]), n * (uint32_t)(kTile * 2));
+    if (a.ld == (int64_t)a.groups_per_token * kTile) {
+      // contiguous rows: the stage is one run of bytes
+      bulk_load(dst, a.x + (size_t)g0 * kTile, n * (uint32_t)(kTile * 2), smem_u32(&sm.full[slot]), pol);
+    } else {
+      // one copy per token row the stage touches
+      for (uint32_t g = g0; g < g0 + n;) {
+        const uint32_t t = g / a.groups_per_token, gin = g - t * a.groups_per_token;
+        const uint32_t len = min(a.groups_per_token - gin, g0 + n - g);
+        bulk_load(dst + (g - g0) * (uint32_t)(kTile * 2), a.x + (int64_t)t * a.ld + (int64_t)gin * kTile,
+                  len * (uint32_t)(kTile * 2), smem_u32(&sm.full[slot]), pol);
+        g += len;
+      }
+    }
   }
   // the CTA must not leave with copies in flight: wait (bounded) for the
   // last entry filled on each slot
@@ -163,10 +182,11 @@ __device__ void ring_producer(const RingArgs& a, RingCtl& sm, uint8_t* stages) {
   }
   if (!a.ticket) return;
   // a CTA that gave up takes the tickets left, so that every CTA ends and
-  // the counter is reset; the last CTA to count itself done resets it
+  // the counter is reset; every ticket taken has landed (its value is used)
+  // before the CTA counts itself done, and the last CTA to do so resets it
   if (failed)
-    while (atomicAdd(a.ticket, 1u) < a.num_stages) {
-    }
+    while (next < a.num_stages) next = atomicAdd(a.ticket, 1u);
+  asm volatile("" ::"r"(next) : "memory");
   __threadfence();
   if (atomicAdd(a.ticket + 1, 1u) == gridDim.x - 1) {
     *reinterpret_cast<volatile uint32_t*>(a.ticket) = 0u;
@@ -335,6 +355,10 @@ __device__ int g_token_error;
 // no ring to fill, measured faster on B300.
 constexpr int kRingMinStagesPerSmTicket = 16;
 constexpr int kRingMinStagesPerSmFixed = 32;
+// Strided rows (x_ld > hidden) take one copy per row segment of a stage;
+// the ring takes them when rows are at least this many groups long (at
+// most five copies per stage), the register kernel otherwise.
+constexpr int64_t kRingMinGroupsPerStridedRow = 32;
 constexpr int kMaxDevices = 64;
 struct DeviceInfo {
   int sm_count = 0;
@@ -409,12 +433,19 @@ extern "C" wt_status wt_quantize_tokens(const void* x, int64_t tokens, int64_t h
                    reinterpret_cast<uintptr_t>(codes) % 8 == 0;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const bool flat = vec && hidden % kTile == 0 && x_ld == hidden;
+  // strided rows go through the ring when a stage touches few of them
+  const bool ring_ok = flat || (vec && hidden % kTile == 0 && gpt >= kRingMinGroupsPerStridedRow);
   const uint32_t num_stages = (num_groups + kRingStageGroups - 1) / kRingStageGroups;
   const uint32_t sms = (uint32_t)di->sm_count;
+  // strided rows measured slower with the ticket counter than with the
+  // fixed hand-out (0.484 against 0.443 ms for 131072 x 7168 rows 7296
+  // apart), so they take the fixed hand-out
   const bool use_ticket = flat && ticket && num_stages >= kRingMinStagesPerSmTicket * sms;
-  if (use_ticket || (flat && num_stages >= kRingMinStagesPerSmFixed * sms)) {
+  if (use_ticket || (ring_ok && num_stages >= kRingMinStagesPerSmFixed * sms)) {
     RingArgs a;
     a.x = static_cast<const uint16_t*>(x);
+    a.ld = x_ld;
+    a.groups_per_token = (uint32_t)gpt;
     a.codes = static_cast<uint8_t*>(codes);
     a.scales = scales;
     a.ticket = use_ticket ? ticket : nullptr;

@@ -350,10 +350,11 @@ wt_status wt_debug_noalloc_stall_unit(int64_t unit, uint64_t wait_limit_ns);
  * scales: tokens x ceil(hidden / 128) fp32, row-major; both caller-owned on
  * the same device. x 2-byte and scales 4-byte aligned; 16-byte-aligned x
  * with hidden and x_ld multiples of 8 (and 8-byte-aligned codes) take the
- * vector path, and of those a contiguous batch (hidden a multiple of 128,
- * x_ld == hidden) is streamed through shared memory by bulk copies, whose
- * waits are bounded: one that gives up leaves that call's output
- * incomplete and is reported by wt_tokens_check.
+ * vector path, and of those a large batch with hidden a multiple of 128
+ * (contiguous, or rows of at least 4096 channels x_ld apart) is streamed
+ * through shared memory by bulk copies, whose waits are bounded: one that
+ * gives up leaves that call's output incomplete and is reported by
+ * wt_tokens_check.
  * ticket: NULL, or two uint32 words of device memory (4-byte aligned) that
  * are zero before the first call that uses them. Large contiguous batches
  * then hand their shared-memory stages to the SMs one at a time from this

@@ -68,17 +68,21 @@ def _ticket():
     return torch.zeros(2, dtype=torch.int32, device="cuda:0")
 
 
-# Contiguous batches of at least 16 (with a ticket counter) or 32 (without)
-# stages of 128 groups per SM go through the shared-memory ring: 16384 x
-# 7168 (48 stages per SM: both), 8192 x 7168 (24: with a ticket), 700001 x
-# 128 (37, last stage 97 groups: both), 300007 x 256 (32 - 0.3, last stage
-# 78 groups: with a ticket). Smaller contiguous batches take the register
-# kernel's flat path (4096 x 7168, 3001 x 7168, 128 x 7168, 1000 x 2048,
-# 17 x 1024, 2 x 128), the rest its strided and element paths. Each case
-# runs with and without a ticket.
+# Batches of at least 16 (with a ticket counter) or 32 (without) stages of
+# 128 groups per SM go through the shared-memory ring: 16384 x 7168 (48
+# stages per SM: both), 8192 x 7168 (24: with a ticket), 700001 x 128 (37,
+# last stage 97 groups: both), 300007 x 256 (32 - 0.3, last stage 78
+# groups: with a ticket); strided rows of at least 32 groups too, one copy
+# per row segment, always handed out per SM: 16384 x 7168 with rows 7296
+# apart, 40001 x 4096 with rows 4104 apart (68 stages per SM, last stage 32
+# groups). Smaller
+# contiguous batches take the register kernel's flat path (4096 x 7168,
+# 3001 x 7168, 128 x 7168, 1000 x 2048, 17 x 1024, 2 x 128), the rest its
+# strided and element paths. Each case runs with and without a ticket.
 @pytest.mark.parametrize("with_ticket", [False, True])
 @pytest.mark.parametrize("tokens,hidden,ld", [(16384, 7168, None), (8192, 7168, None), (700001, 128, None),
-                                              (300007, 256, None), (4096, 7168, None), (3001, 7168, None),
+                                              (300007, 256, None), (16384, 7168, 7296), (40001, 4096, 4104),
+                                              (4096, 7168, None), (3001, 7168, None),
                                               (128, 7168, None), (1000, 2048, None), (17, 1024, None),
                                               (257, 7168, 7680), (5, 200, None), (3, 130, None),
                                               (7, 1000, 1003), (1, 1, None), (2, 128, None)])
