@@ -424,10 +424,11 @@ wt_status compile_plan(const wt_plan_desc* d, Plan* p) {
   }
   p->num_dst_entries = dst_entries;
   p->num_units = (int64_t)p->h_units.size();
-  // Units whose rows are gathered one bulk copy per row (rows from several
-  // shards, or rows that are not 16-byte aligned) take several times as
-  // long as a tensor-copied block; a launch hands them out first, so that
-  // they overlap the streaming blocks instead of forming its tail.
+  // Units whose rows are gathered row by row (rows from several shards, or
+  // rows that are not 16-byte aligned: a bulk copy per row, or loads by the
+  // consumers from published row addresses) take longer than a
+  // tensor-copied block; a launch hands them out first, so that they
+  // overlap the streaming blocks instead of forming its tail.
   auto slow = [&](int64_t u) {
     const uint32_t f = p->h_units[(size_t)u].shape >> 16;
     return (f & kUnitMulti) || !(f & kUnitVec);
