@@ -13,20 +13,20 @@
 // through a TMA ring: the batch's groups, in token order, are cut into
 // stages of 128 groups (32 KiB; the last may be shorter), each copied with
 // one bulk copy when rows are contiguous (x_ld == hidden), else one per
-// token row it touches (rows of at least 32 groups).
-// A producer warp per CTA (one CTA per SM) copies stages into a ring of
-// shared-memory slots with cp.async.bulk and tells the consumers which
-// stage each slot holds; two consumer groups of twelve warps take alternate
-// slots, quantise from shared memory and store codes and scales straight
-// to global memory. With a caller's ticket counter the producers of a
-// contiguous batch take stages from it one at a time, each ticket a stage
-// ahead (SMs that are served faster take more; the last CTA resets it), six
-// slots deep; otherwise CTA b takes stages b, b + gridDim.x, ..., four
-// slots deep (a deeper ring measured slower with the fixed hand-out). Lane l of group j reads chunk 4 ((c + j) mod 4) +
-// l % 4 at step c, so that the two groups in each 8-lane phase of a
-// 16-byte shared load fall in different bank halves. Every wait is
-// bounded; the role that gives up records kErrTimeout in the codec's error
-// word (wt_tokens_check).
+// token row it touches (rows of at least 32 groups). A producer warp per
+// CTA (one CTA per SM) copies stages into a ring of shared-memory slots
+// with cp.async.bulk and tells the consumers which stage each slot holds;
+// two consumer groups of twelve warps take alternate slots, quantise from
+// shared memory and store codes and scales straight to global memory. With
+// a caller's ticket counter the producers of a contiguous batch take
+// stages from it one at a time, each ticket a stage ahead (SMs that are
+// served faster take more; the last CTA resets it), six slots deep;
+// otherwise CTA b takes stages b, b + gridDim.x, ..., four slots deep (a
+// deeper ring measured slower with the fixed hand-out). Lane l of group j
+// reads chunk 4 ((c + j) mod 4) + l % 4 at step c, so that the two groups
+// in each 8-lane phase of a 16-byte shared load fall in different bank
+// halves. Every wait is bounded; the role that gives up records
+// kErrTimeout in the codec's error word (wt_tokens_check).
 //
 // Smaller batches, and all other shapes (hidden not a multiple of 128,
 // short strided rows, unaligned x), use a register-streaming kernel, which
@@ -68,7 +68,7 @@ __device__ __forceinline__ float group_scale(const uint4 (&v)[kTokChunks]) {
   return amax == 0.0f ? 1.0f : __fdiv_rn(amax, 448.0f);
 }
 
-// --------------------------------------------------- contiguous: TMA ring ---
+// ------------------------------------------------- large batches: TMA ring ---
 constexpr int kRingGroupWarps = 12;                  // warps per consumer group
 constexpr int kRingGroups = 2;                       // consumer groups: ring entry i -> group i % 2
 constexpr int kRingSlots = 6;                        // shared-memory slots (the deepest ring used)
@@ -350,9 +350,9 @@ __global__ void __launch_bounds__(kTokThreads) token_kernel(const __grid_constan
 // wait that gave up, read and cleared by wt_tokens_check.
 __device__ int g_token_error;
 
-// The ring takes a contiguous batch from this many stages per SM on (with
-// a ticket counter, else without): below, the register kernel, which needs
-// no ring to fill, measured faster on B300.
+// The ring takes a batch from this many stages per SM on (contiguous with
+// a ticket counter, else any): below, the register kernel, which needs no
+// ring to fill, measured faster on B300.
 constexpr int kRingMinStagesPerSmTicket = 16;
 constexpr int kRingMinStagesPerSmFixed = 32;
 // Strided rows (x_ld > hidden) take one copy per row segment of a stage;
