@@ -36,6 +36,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -52,23 +53,33 @@ L2_BYTES = 126 * 10**6
 # dram__bytes_read.sum + dram__bytes_write.sum of one prep_kernel launch,
 # from the ncu capture summarised in profiles/ (16 experts, scaled by the
 # blocks processed to the 385-expert layer); valid only for the kernel
-# source it was taken on.
-TRAFFIC = {"kernel_sha256": "b74545c16da840cd3e3e88f261b0b76e733f80f5c554748701861753f1b1d707",
+# code it was taken on (kernel_sha).
+TRAFFIC = {"kernel_sha256": "73bf6d89e7c66e3677cfb3b9597b05c0ec65785b264b71f8e581580bb54995e0",
            "bytes_per_launch": 50029567280, "experts": 385}
 
 
+_COMMENT_OR_STRING = re.compile(rb'("(?:\\.|[^"\\\n])*")|//[^\n]*|/\*.*?\*/', re.S)
+
+
+def _code_only(src: bytes) -> bytes:
+    """C++ source with its comments removed and whitespace collapsed, so
+    that editing a comment does not change what it hashes to."""
+    src = _COMMENT_OR_STRING.sub(lambda m: m.group(1) or b" ", src)
+    return b" ".join(src.split())
+
+
 def kernel_sha() -> str:
-    """Hash of the preparation kernel's device sources: the kernel, the
-    codec, the PTX primitives and the device part of plan.h (constants,
-    table records, launch arguments; the host-side plan structures after
-    them do not reach the kernel)."""
+    """Hash of the preparation kernel's device code: the kernel, the codec,
+    the PTX primitives and the device part of plan.h (constants, table
+    records, launch arguments; the host-side plan structures after them do
+    not reach the kernel), comments and whitespace aside."""
     h = hashlib.sha256()
     for name in ("prep_kernel.cu", "codec.cuh", "ptx.cuh", "plan.h"):
         with open(os.path.join(ROOT, "bf16_fp8_parameter_wt_b300", "csrc", name), "rb") as f:
             src = f.read()
         if name == "plan.h":
             src = src[:src.index(b"// Host-side copy of one param.")]
-        h.update(src)
+        h.update(_code_only(src))
     return h.hexdigest()
 
 

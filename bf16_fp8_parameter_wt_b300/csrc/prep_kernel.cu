@@ -19,15 +19,15 @@
 //     34 KiB shared-memory stages with the tensor memory accelerator: one
 //     2-D tensor copy when all 128 rows come from one shard and are 16-byte
 //     aligned; for rows that are not, k tensor copies through the shard's
-//     view map (k shard rows per view row, see tmap.cpp); otherwise one 1-D
-//     bulk copy per row (the full_tensor() row gather across shards, or
-//     unaligned rows without a view map). Blocks of 16-byte rows from
-//     several shards, and blocks of rows at most 8 elements wide, are not
-//     copied at all: the producer publishes each row's address in the
-//     stage and the consumers load their chunks themselves (128 small bulk
-//     copies cost about 5 us per block). Full/empty mbarriers order the
-//     ring; the producer runs up to four units ahead, so HBM reads stay in
-//     flight while the consumers compute.
+//     view map (k shard rows per view row, see tmap.cpp). The full_tensor()
+//     row gather across shards of 16-byte rows, and blocks of rows at most
+//     8 elements wide, take no copy: the producer publishes each row's
+//     address in the stage and the consumers load their chunks themselves
+//     (128 small bulk copies cost about 5 us per block). The rest (wider
+//     unaligned rows from several shards or without a view map) take one
+//     1-D bulk copy per row. Full/empty mbarriers order the ring; the
+//     producer runs up to four units ahead, so HBM reads stay in flight
+//     while the consumers compute.
 //   - two consumer groups of four warps take alternate units. Thread t of a
 //     group owns the 16-byte column chunk t % 16 of the rows t / 16 + 8 j,
 //     j = 0..15: it loads them from shared memory (conflict-free, two full
@@ -140,14 +140,16 @@ __device__ __forceinline__ Batch load_batch(const PrepArgs& a, bool dyn, int64_t
   return bt;
 }
 
-// Rows from several shards, or rows that are not 16-byte aligned without a
-// view map: one bulk copy per row (the full_tensor() row gather). A
-// 16-byte-aligned row lands at its place in the stage; any other row is
-// copied as the 16-byte-aligned span that holds it into its 272-byte slot,
-// at offset address % 16 (the span starts at most 15 bytes before the row
-// and ends at most 15 after it; both ends lie in the 16-byte granules of
-// the row's own first and last bytes, so no page that the row does not
-// touch is read), and the consumers move it into place.
+// Rows that are not 16-byte aligned (or treated as such under
+// WT_FLAG_FORCE_NARROW), wider than 8 elements, from several shards or
+// without a view map: one bulk copy per row. Each row is copied as the
+// 16-byte-aligned span that holds it into its 272-byte slot, at offset
+// address % 16 (the span starts at most 15 bytes before the row and ends
+// at most 15 after it; both ends lie in the 16-byte granules of the row's
+// own first and last bytes, so no page that the row does not touch is
+// read), and the consumers move it into place. Blocks of 16-byte rows take
+// tensor copies or direct loads, so the branch below that would copy such
+// a row straight to its place in the stage serves no current unit.
 __device__ __forceinline__ void load_rows(const PrepArgs& a, SmemCtl& sm, const uint32_t (&w)[8], int st,
                                           uint32_t dst, uint32_t full, uint64_t pol, int lane) {
   const int nrows = (int)(w[5] & 0xFFu) + 1;

@@ -57,3 +57,15 @@ def test_rank_groups_counts_the_launches_of_a_step_counted_per_rank():
     # every block there has a destination on rank 0 (a whole-tensor replica,
     # or a row slice covering every row): one group
     assert bench.rank_groups(tp_slices_small()) == 1
+
+
+def test_kernel_hash_ignores_comments_and_whitespace_only():
+    """The traffic figure stays tied to the kernel's code: comments and
+    layout do not change the hash, code (string literals included) does."""
+    base = b'asm volatile("ld.global.nc.v4.u32 {%0}, [%1];");\nint a = 1;  // one\n'
+    same = b'/* a block\n comment */ asm volatile("ld.global.nc.v4.u32 {%0}, [%1];");\n\n  int a = 1; // two\n'
+    assert bench._code_only(base) == bench._code_only(same)
+    assert bench._code_only(base) != bench._code_only(base.replace(b"a = 1", b"a = 2"))
+    assert bench._code_only(base) != bench._code_only(base.replace(b"v4.u32", b"v2.u32"))
+    kept = bench._code_only(b'const char* s = "a // b /* c */";')
+    assert kept == b'const char* s = "a // b /* c */";'
