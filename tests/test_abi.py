@@ -207,6 +207,11 @@ def test_token_codec_validates_arguments_before_touching_a_device():
     assert L.wt_quantize_tokens(2, 1 << 25, 1 << 13, 1 << 13, 16, 16, None, None) == 1  # > 2^31 groups
     align = wt.lib().wt_status_string
     assert align(L.wt_quantize_tokens(2, 4, 128, 128, 16, 16, 6, None)) == b"WT_ERR_ALIGNMENT"  # ticket
+    # the testing hook of the codec's bounded waits: -1 (off) and groups >= 0
+    # are accepted, anything below -1 refused, all without a device
+    assert L.wt_debug_tokens_stall_group(-2, 0) == 1
+    assert L.wt_debug_tokens_stall_group(5, 1000) == 0
+    assert L.wt_debug_tokens_stall_group(-1, 0) == 0
 
 
 @pytest.mark.parametrize("make", [tiny_dense, llama_dense_tp4, tp_slices_small,
