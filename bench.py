@@ -351,6 +351,34 @@ def cpu_baseline(w_full, experts_sample: int, steps: int = 3) -> dict:
                                         f"({one.num_params_total} params), one run, {t1:.2f} s"}}
 
 
+def token_cpu_baseline(tokens: int, hidden: int, steps: int = 3) -> dict:
+    """Time the CPU oracle's 1 x 128 codec, as it stands, on a seeded
+    sample of the batch (same hidden size and value recipe), its tokens
+    split over the host cores: the median of `steps` runs."""
+    from concurrent.futures import ThreadPoolExecutor
+    import numpy as np
+    import torch
+    import oracle
+    oracle.build()
+    g = torch.Generator().manual_seed(1006)
+    z = torch.randn(tokens, hidden, generator=g)
+    chi = sum(torch.randn(tokens, hidden, generator=g) ** 2 for _ in range(3))
+    bits = (z * 0.02 / torch.sqrt(chi / 3)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    del z, chi
+    cores = host_cores()
+    chunks = [c for c in np.array_split(np.arange(tokens), cores) if c.size]
+    times = []
+    with ThreadPoolExecutor(len(chunks)) as ex:
+        for _ in range(steps):
+            t0 = time.perf_counter()
+            list(ex.map(lambda ix: oracle.quantize_tokens(bits[ix[0]:ix[-1] + 1]), chunks))
+            times.append(time.perf_counter() - t0)
+    t = statistics.median(times)
+    return {"value": round(2 * tokens * hidden / t / 1e9, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": f"{tokens} tokens x {hidden} (same recipe), split over {len(chunks)} threads, "
+                      f"median of {steps} run(s), {t:.2f} s each"}
+
+
 def run_reference(args, world, rank):
     """The reference arm: the CPU oracle timed on the host cores."""
     if rank != 0:
@@ -420,6 +448,8 @@ def main():
     ap.add_argument("--counters", choices=["launch", "rank"], default=None,
                     help="time the step with per-rank completion counters")
     ap.add_argument("--tokens", type=int, default=131072)
+    ap.add_argument("--cpu-tokens", type=int, default=32768,
+                    help="tokens of the sample the CPU oracle is timed on (--workload tokens)")
     ap.add_argument("--hidden", type=int, default=7168)
     ap.add_argument("--images", type=int, default=2)
     ap.add_argument("--stack-steps", type=int, default=2)
@@ -717,6 +747,9 @@ def run_tokens(args, world, rank, local):
     del graph, x, codes, scales
     torch.cuda.empty_cache()
     mix = mix_2to1_peak(dev, stream)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = token_cpu_baseline(min(args.cpu_tokens, T), H)
     line = {
         "metric": "wt_quantize_tokens GB/s (BF16 in), 1x128 e4m3 activation codec",
         "value": round(world * bytes_in / (ms * 1e-3) / 1e9, 2), "unit": "GB/s", "n_gpus": world,
@@ -732,7 +765,7 @@ def run_tokens(args, world, rank, local):
                      "launch_ms_median": round(statistics.median(per), 4),
                      "mix_2to1_peak": round(mix, 1), "frac_of_mix_2to1_peak": round(achieved / mix, 4)},
         "dispatch_128_tokens_us": round(small[0].elapsed_time(small[1]) * 1e3 / reps, 2),
-        "clocks": clk, "gpu_launches": args.steps,
+        "cpu_baseline": cpu, "clocks": clk, "gpu_launches": args.steps,
     }
     if rank == 0:
         print(json.dumps(line), flush=True)

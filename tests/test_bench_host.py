@@ -69,3 +69,9 @@ def test_kernel_hash_ignores_comments_and_whitespace_only():
     assert bench._code_only(base) != bench._code_only(base.replace(b"v4.u32", b"v2.u32"))
     kept = bench._code_only(b'const char* s = "a // b /* c */";')
     assert kept == b'const char* s = "a // b /* c */";'
+
+
+def test_token_cpu_baseline_record(oracle_mod):
+    rec = bench.token_cpu_baseline(64, 256, steps=1)
+    assert rec["kind"] == "oracle" and rec["unit"] == "GB/s" and rec["value"] > 0
+    assert rec["cores"] >= 1 and "64 tokens x 256" in rec["sample"]
