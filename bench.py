@@ -635,7 +635,9 @@ def main():
         torch.cuda.empty_cache()
         e2e = measure_e2e(w, shards, args, dev, world)
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline and partition == "replicas":
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        # the oracle on a sample of the whole workload, whichever share of it
+        # the partition gives this rank
         del shards, flat
         torch.cuda.empty_cache()
         cpu = cpu_baseline(w, args.cpu_experts)
