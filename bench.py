@@ -928,6 +928,9 @@ def run_offload_stack(args, world, rank, local):
     dt = max_over_ranks(world, dt, dev)
     peak = h2d_peak(images[0], dev, copy_s)
     plan.close()
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w, args.cpu_experts)
     host_bytes = layers * st["host_bytes"]
     value = world * layers * st["bytes_read"] / dt / 1e9
     line = {
@@ -944,7 +947,7 @@ def run_offload_stack(args, world, rank, local):
                 "d2h_bytes_per_step": 4},
         "h2d_peak_gbs": round(peak, 2),
         "overlap_efficiency": round(host_bytes / (peak * 1e9) / dt, 4),
-        "clocks": clk,
+        "cpu_baseline": cpu, "clocks": clk,
         # one preparation launch per chunk of every layer
         "gpu_launches": args.stack_steps * layers * st["num_chunks"],
     }
